@@ -1,0 +1,135 @@
+"""Seeded synthetic MoE layers: shapes, value distributions and the host-side generator.
+
+Every tensor is drawn from its own Philox stream (see ``synth.philox``) keyed by
+(seed, instance), with counter words (element block, expert, tensor id), so that any
+expert of any instance can be regenerated on its own, on the host or on the device.
+
+Recipe (all layers):
+* x       bf16 [T, H]   : N(0, 1) rounded to bf16 (nearest-even)
+* logits  fp32 [T, E]   : N(0, sigma_logits^2); with ``expert_bias`` a per-expert
+                          N(0, 1) bias is added (fp32 add) before routing
+* W13     [E, 2I, H]    : fp32 N(0, 0.02^2), gate rows [0, I) then up rows [I, 2I),
+                          quantised to NVFP4 along H, one tensor scale per expert
+* W2      [E, H, I]     : fp32 N(0, 0.02^2), quantised along I, one tensor scale per expert
+* shared expert (optional): dense W13s [2I, H], W2s [H, I] with the same recipe and a
+                          gate vector gv bf16 [H] ~ N(0, 0.02^2)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import philox as px
+from .quantize import f32_to_bf16_bits, quantize_nvfp4
+
+
+@dataclass(frozen=True)
+class LayerSpec:
+    name: str
+    seed: int
+    T: int
+    E: int
+    k: int
+    H: int
+    I: int
+    logit_sigma: float = 1.0
+    shared: bool = False
+    expert_bias: bool = False
+    instances: int = 1
+    w_sigma: float = 0.02
+    x_sigma: float = 1.0
+    swiglu_limit: float = 7.0
+    prefill: bool = False
+
+
+# The five workloads of the layer (shapes as stated for the MoE layer under test).
+TINY = LayerSpec("tiny_t1_e8_k2_h256_i128", seed=0, T=1, E=8, k=2, H=256, I=128,
+                 logit_sigma=1.0)
+DECODE_B1_E288 = LayerSpec("decode_t1_e288_k8_h3072_i1024", seed=1, T=1, E=288, k=8,
+                           H=3072, I=1024, logit_sigma=1.5, instances=48)
+DECODE_B1_E512 = LayerSpec("decode_t1_e512_k10_h4096_i1024_shared", seed=2, T=1, E=512,
+                           k=10, H=4096, I=1024, logit_sigma=1.5, shared=True,
+                           instances=48)
+DECODE_B32_E512 = LayerSpec("decode_t32_e512_k10_h4096_i1024_shared", seed=3, T=32,
+                            E=512, k=10, H=4096, I=1024, logit_sigma=1.5, shared=True)
+PREFILL_T2048 = LayerSpec("prefill_t2048_e512_k10_h4096_i1024", seed=4, T=2048, E=512,
+                          k=10, H=4096, I=1024, logit_sigma=1.5, expert_bias=True,
+                          prefill=True)
+
+WORKLOADS = [TINY, DECODE_B1_E288, DECODE_B1_E512, DECODE_B32_E512, PREFILL_T2048]
+BY_NAME = {s.name: s for s in WORKLOADS}
+
+
+def gen_x(spec: LayerSpec, instance: int = 0) -> np.ndarray:
+    z = px.normals(spec.seed, instance, px.TID_X, 0, spec.T * spec.H, spec.x_sigma)
+    return f32_to_bf16_bits(z).reshape(spec.T, spec.H)
+
+
+def gen_logits(spec: LayerSpec, instance: int = 0) -> np.ndarray:
+    lg = px.normals(spec.seed, instance, px.TID_LOGITS, 0, spec.T * spec.E,
+                    spec.logit_sigma).reshape(spec.T, spec.E)
+    if spec.expert_bias:
+        bias = px.normals(spec.seed, instance, px.TID_BIAS, 0, spec.E, 1.0)
+        lg = (lg + bias[None, :]).astype(np.float32)
+    return lg
+
+
+def gen_gate(spec: LayerSpec, instance: int = 0) -> np.ndarray:
+    z = px.normals(spec.seed, instance, px.TID_GATE, 0, spec.H, spec.w_sigma)
+    return f32_to_bf16_bits(z)
+
+
+def gen_w13_fp32(spec: LayerSpec, instance: int, e: int, tid: int = px.TID_W13):
+    n = 2 * spec.I * spec.H
+    return px.normals(spec.seed, instance, tid, e, n, spec.w_sigma).reshape(2 * spec.I, spec.H)
+
+
+def gen_w2_fp32(spec: LayerSpec, instance: int, e: int, tid: int = px.TID_W2):
+    n = spec.H * spec.I
+    return px.normals(spec.seed, instance, tid, e, n, spec.w_sigma).reshape(spec.H, spec.I)
+
+
+def gen_expert(spec: LayerSpec, instance: int, e: int, shared: bool = False):
+    """Quantised weights of one expert: (w13, s13, g13, w2, s2, g2)."""
+    t13 = px.TID_W13_SHARED if shared else px.TID_W13
+    t2 = px.TID_W2_SHARED if shared else px.TID_W2
+    w13, s13, g13 = quantize_nvfp4(gen_w13_fp32(spec, instance, e, t13))
+    w2, s2, g2 = quantize_nvfp4(gen_w2_fp32(spec, instance, e, t2))
+    return w13, s13, g13, w2, s2, g2
+
+
+@dataclass
+class Layer:
+    """One synthetic layer instance in host memory (numpy)."""
+    spec: LayerSpec
+    x: np.ndarray            # uint16 bf16 bits [T, H]
+    logits: np.ndarray       # float32 [T, E]
+    w13: np.ndarray          # uint8 [E, 2I, H/2]
+    s13: np.ndarray          # uint8 [E, 2I, H/16]
+    g13: np.ndarray          # float32 [E]
+    w2: np.ndarray           # uint8 [E, H, I/2]
+    s2: np.ndarray           # uint8 [E, H, I/16]
+    g2: np.ndarray           # float32 [E]
+    shared: dict | None = None   # keys w13 s13 g13 w2 s2 g2 gate
+    extra: dict = field(default_factory=dict)
+
+
+def make_layer(spec: LayerSpec, instance: int = 0) -> Layer:
+    """Generate a whole layer on the host. Meant for the small shapes (seconds of CPU)."""
+    E, H, I = spec.E, spec.H, spec.I
+    w13 = np.empty((E, 2 * I, H // 2), np.uint8)
+    s13 = np.empty((E, 2 * I, H // 16), np.uint8)
+    g13 = np.empty(E, np.float32)
+    w2 = np.empty((E, H, I // 2), np.uint8)
+    s2 = np.empty((E, H, I // 16), np.uint8)
+    g2 = np.empty(E, np.float32)
+    for e in range(E):
+        w13[e], s13[e], g13[e], w2[e], s2[e], g2[e] = gen_expert(spec, instance, e)
+    shared = None
+    if spec.shared:
+        a, b, c, d, f, g = gen_expert(spec, instance, 0, shared=True)
+        shared = dict(w13=a, s13=b, g13=np.float32(c), w2=d, s2=f, g2=np.float32(g),
+                      gate=gen_gate(spec, instance))
+    return Layer(spec, gen_x(spec, instance), gen_logits(spec, instance),
+                 w13, s13, g13, w2, s2, g2, shared)
