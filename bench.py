@@ -1,0 +1,426 @@
+"""Benchmark of the NVFP4 MoE layer on GB300: one JSON line on stdout (rank 0).
+
+A step is one layer call: router (ft_moe_route) + experts (ft_moe_nvfp4_decode, or
+ft_moe_nvfp4_prefill for the prefill workload) on one synthetic layer instance. The
+decode workloads rotate over 48 distinct instances (weights far larger than L2, so every
+call streams its experts from HBM); the timed loop replays a CUDA graph of one pass over
+the instances.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (the plain float32 reference) on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 MoE layer µs/call & achieved HBM GB/s vs GB300 peak (batch 1–32)"
+DEFAULT_WORKLOAD = "decode_t1_e288_k8_h3072_i1024"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+NVFP4_BYTES_PER_ELEM = 0.5625       # 4-bit code + one E4M3 byte per 16 elements
+
+
+# ----------------------------------------------------------------------- helpers
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=480)
+    ap.add_argument("--warmup", type=int, default=48)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--instances", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, bf16, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = o
+            walk(d)
+            for k, v in flat.items():
+                kl = k.lower()
+                if isinstance(v, (int, float)) and "hbm" in kl and "gbs" in kl:
+                    hbm, src = float(v), "measured"
+                if isinstance(v, (int, float)) and kl.endswith("bf16_tflops"):
+                    bf16 = float(v)
+        except Exception:
+            pass
+    return hbm, bf16, src
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
+                                          f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def layer_bytes(spec, n_experts_touched: int) -> float:
+    """Algorithmic HBM bytes of one layer call: every touched expert's NVFP4 W13 and W2
+    (codes + block scales) and its two tensor scales, plus x, logits, gate and output."""
+    per_expert = 3 * spec.H * spec.I * NVFP4_BYTES_PER_ELEM + 8
+    n = n_experts_touched + (1 if spec.shared else 0)
+    io = spec.T * spec.H * 2 * 2 + spec.T * spec.E * 4 + (spec.H * 2 if spec.shared else 0)
+    return n * per_expert + io
+
+
+def layer_flops(spec, n_pairs: int) -> float:
+    return 2.0 * n_pairs * 3 * spec.H * spec.I
+
+
+# ------------------------------------------------------------------ our implementation
+def run_ours(args, spec, rank, world, local):
+    import torch
+    from nvfp4_mixture_experts_02_gb300 import ftmoe
+    from synth.device import make_device_layer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n_inst = args.instances or spec.instances
+    prefill = spec.prefill
+    layers, exps, shs, wss, idxs, ws_ = [], [], [], [], [], []
+    touched, pairs = [], []
+    for i in range(n_inst):
+        lay = make_device_layer(spec, instance=rank * n_inst + i, device=dev)
+        ex = ftmoe.NvFP4Experts(lay.w13, lay.s13, lay.g13, lay.w2, lay.s2, lay.g2)
+        sh = None
+        if lay.shared is not None:
+            s = lay.shared
+            sh = ftmoe.NvFP4Shared(s["w13"], s["s13"], s["g13"], s["w2"], s["s2"], s["g2"],
+                                   s["gate"])
+        idx = torch.empty((spec.T, spec.k), dtype=torch.int32, device=dev)
+        w = torch.empty((spec.T, spec.k), dtype=torch.float32, device=dev)
+        ftmoe.route(lay.logits, spec.k, idx, w)
+        torch.cuda.synchronize()
+        touched.append(int(torch.unique(idx).numel()))
+        pairs.append(spec.T * spec.k)
+        layers.append(lay)
+        exps.append(ex)
+        shs.append(sh)
+        idxs.append((idx, w))
+    ws = ftmoe.new_workspace(spec.T, spec.k, exps[0], spec.shared, prefill=prefill)
+    outs = [torch.empty((spec.T, spec.H), dtype=torch.bfloat16, device=dev) for _ in range(n_inst)]
+    call = ftmoe.prefill if prefill else ftmoe.decode
+
+    def step(i, with_route=True):
+        lay = layers[i]
+        idx, w = idxs[i]
+        if with_route:
+            ftmoe.route(lay.logits, spec.k, idx, w)
+        call(lay.x, idx, w, exps[i], shs[i], limit=spec.swiglu_limit, out=outs[i], workspace=ws)
+
+    # warm up eagerly (also sets kernel attributes outside capture)
+    for i in range(min(n_inst, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert ftmoe.get_error(ws) == 0
+
+    stream = torch.cuda.Stream(device=dev)
+    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_step, stream=stream):
+            for i in range(n_inst):
+                step(i)
+        with torch.cuda.graph(g_dec, stream=stream):
+            for i in range(n_inst):
+                step(i, with_route=False)
+    torch.cuda.synchronize()
+
+    passes_w = max(1, (args.warmup + n_inst - 1) // n_inst)
+    passes_k = max(1, (args.steps + n_inst - 1) // n_inst)
+    steps_done = passes_k * n_inst
+    for _ in range(passes_w):
+        g_step.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        ev0.record()
+        for _ in range(passes_k):
+            g_step.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        step_ms = ev0.elapsed_time(ev1)
+        # decode-only replays: the expert kernels' duration for the roofline
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record()
+        for _ in range(passes_k):
+            g_dec.replay()
+        d1.record()
+        torch.cuda.synchronize()
+        dec_ms = d0.elapsed_time(d1)
+    assert ftmoe.get_error(ws) == 0
+    step_ms = max_over_ranks(step_ms, world)
+
+    bytes_call = statistics.mean(layer_bytes(spec, t) for t in touched)
+    flops_call = statistics.mean(layer_flops(spec, p) for p in pairs)
+    us_call = step_ms * 1e3 / steps_done
+    dec_us = dec_ms * 1e3 / steps_done
+    total_bytes = bytes_call * steps_done * world
+    gbs = total_bytes / (step_ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world)
+
+    hbm, bf16, src = measured_peaks()
+    if prefill:
+        achieved = flops_call / (dec_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": None,
+                "peak_source": src, "kernel": "ft_moe_nvfp4_prefill"}
+    else:
+        achieved = bytes_call / (dec_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
+                "kernel": "ft_moe_nvfp4_decode (plan + W13/SwiGLU + W2/sum kernels)",
+                "us_per_launch": round(dec_us, 3)}
+    res = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": steps_done, "warmup": passes_w * n_inst, "ms_per_step": step_ms / steps_done,
+        "us_per_call": round(us_call, 3), "tokens_per_s": round(spec.T * steps_done * world /
+                                                                 (step_ms * 1e-3), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights (e2m1 x e4m3 -> f16), f16 mma, f32 accumulate, bf16 in/out",
+        "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, N(0,1) bf16 x)",
+        "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k, "H": spec.H,
+                   "I": spec.I, "shared_expert": spec.shared, "instances": n_inst,
+                   "l2": f"inputs larger than L2: {n_inst} distinct layer instances rotated",
+                   "graph": "CUDA graph of one pass over the instances",
+                   "bytes_per_call": round(bytes_call), "experts_touched_mean":
+                   statistics.mean(touched)},
+        "roofline": roof, "e2e": e2e, "gpu_launches": 4 * steps_done,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(spec, layers[:2], bytes_call)
+    return res
+
+
+def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
+    import torch
+    from nvfp4_mixture_experts_02_gb300 import ftmoe
+    n = min(len(layers), 48)
+    hx = [torch.from_numpy(l.x_bits.view(np.int16)).pin_memory() for l in layers[:n]]
+    hl = [torch.from_numpy(l.logits_np).pin_memory() for l in layers[:n]]
+    hout = torch.empty((spec.T, spec.H), dtype=torch.int16).pin_memory()
+    dx = torch.empty((spec.T, spec.H), dtype=torch.int16, device=dev)
+    dl = torch.empty((spec.T, spec.E), dtype=torch.float32, device=dev)
+    out = torch.empty((spec.T, spec.H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((spec.T, spec.k), dtype=torch.int32, device=dev)
+    w = torch.empty((spec.T, spec.k), dtype=torch.float32, device=dev)
+    call = ftmoe.prefill if spec.prefill else ftmoe.decode
+
+    def one(i):
+        dx.copy_(hx[i], non_blocking=True)
+        dl.copy_(hl[i], non_blocking=True)
+        ftmoe.route(dl, spec.k, idx, w)
+        call(dx.view(torch.bfloat16), idx, w, exps[i], shs[i], limit=spec.swiglu_limit, out=out,
+             workspace=ws)
+        hout.copy_(out.view(torch.int16), non_blocking=True)
+
+    for i in range(min(n, 3)):
+        one(i)
+    torch.cuda.synchronize()
+    steps = max(n, min(args.steps, 4 * n))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        one(s % n)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    return {"value": round(bytes_call * steps * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "us_per_call": round(ms * 1e3 / steps, 3),
+            "h2d_bytes_per_step": spec.T * spec.H * 2 + spec.T * spec.E * 4,
+            "d2h_bytes_per_step": spec.T * spec.H * 2}
+
+
+# --------------------------------------------------------------------- CPU oracle arm
+def oracle_call_seconds(spec, lay, tokens=None):
+    from oracle import moe as om
+    from synth.device import HostExperts
+    host = HostExperts(lay)
+    if tokens is None:
+        tokens = np.arange(spec.T)
+    idx = np.argsort(-lay.logits_np[tokens], axis=1, kind="stable")[:, :spec.k]
+    for e in np.unique(idx):                  # fetch first: device reads are not timed
+        host._fetch(int(e))
+    sh = host.shared_host()
+    t0 = time.perf_counter()
+    om.moe_layer(lay.x_bits, lay.logits_np, spec.k, host, shared=sh, tokens=tokens)
+    return time.perf_counter() - t0, len(tokens)
+
+
+def cpu_baseline(spec, layers, bytes_call):
+    secs, calls = 0.0, 0
+    tokens = None if spec.T <= 32 else np.arange(32)
+    deadline = time.perf_counter() + 20.0
+    while calls < 2 * len(layers) and time.perf_counter() < deadline:
+        s, ntok = oracle_call_seconds(spec, layers[calls % len(layers)], tokens)
+        secs += s * (spec.T / ntok)            # scale a token sample to a whole call
+        calls += 1
+    per_call = secs / max(calls, 1)
+    return {"value": round(bytes_call / per_call / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "us_per_call": round(per_call * 1e6, 1),
+            "sample": f"{calls} layer calls of instances 0-{len(layers) - 1}"
+                      + ("" if tokens is None else f" ({len(tokens)} of {spec.T} tokens, scaled)")
+                      + "; numpy float32, BLAS threads default"}
+
+
+def run_reference(args, spec, rank, world, local):
+    if rank != 0:
+        return None
+    import torch
+    from synth.device import make_device_layer
+    torch.cuda.set_device(local)
+    n_inst = min(args.instances or spec.instances, 4)
+    layers = [make_device_layer(spec, instance=i) for i in range(n_inst)]
+    torch.cuda.synchronize()
+    tokens = None if spec.T <= 32 else np.arange(16)
+    for s in range(args.warmup):
+        oracle_call_seconds(spec, layers[s % n_inst], tokens)
+    total, ntoks = 0.0, 0
+    K = max(1, min(args.steps, 20))
+    for s in range(K):
+        sec, nt = oracle_call_seconds(spec, layers[s % n_inst], tokens)
+        total += sec * (spec.T / nt)
+    per_call = total / K
+    touched = [len(np.unique(np.argsort(-l.logits_np, axis=1, kind="stable")[:, :spec.k]))
+               for l in layers]
+    bytes_call = statistics.mean(layer_bytes(spec, t) for t in touched)
+    v = bytes_call / per_call / 1e9
+    sample = (f"{K} layer calls over instances 0-{n_inst - 1}"
+              + ("" if tokens is None else f", {len(tokens)} of {spec.T} tokens per call, scaled"))
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": per_call * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 (oracle)", "data": "synthetic",
+            "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k,
+                       "H": spec.H, "I": spec.I, "shared_expert": spec.shared},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------ plumbing
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    from synth import BY_NAME
+    spec = BY_NAME[args.workload]
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        res = run_reference(args, spec, rank, world, local)
+    else:
+        res = run_ours(args, spec, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

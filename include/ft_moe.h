@@ -1,0 +1,153 @@
+/*
+ * ft_moe.h — C ABI of the NVFP4 mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * The layer is the one a serving engine runs in every layer at every decode step
+ * (FreeToken PR #84, "Effect in production": the NVFP4 MoE decode GEMV): router
+ * softmax / top-k (FreeToken commit log, 512-expert entry: "non-power-of-2 top-k
+ * router"), then per selected expert a W13 (gate|up) product on NVFP4 weights fused
+ * with clamped SwiGLU (288-expert entry: "clamped-SwiGLU activation across the MoE
+ * stack"), then a W2 product whose outputs are summed with the router weights, plus an
+ * optional gated shared expert (512-expert entry: "512 NVFP4 ... routed experts
+ * (top-10) plus a gated shared expert").
+ *
+ * Conventions for every entry point
+ *  - All array pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing, frees nothing and never synchronises inside route / decode / prefill.
+ *  - bf16 tensors are passed as uint16_t bit patterns (the upper half of an IEEE float).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Work is enqueued
+ *    asynchronously on it; the call returns after enqueueing.
+ *  - Host-side argument checks run before any launch; on failure nothing is enqueued
+ *    and the call returns the error. A failed launch returns FT_ERR_CUDA.
+ *  - Anomalies seen inside kernels (an expert id outside [0, E)) are OR-ed into an
+ *    error word at the start of the workspace; ft_moe_get_error() reports and clears it.
+ *  - Results are deterministic: the same inputs give the same output bits.
+ *
+ * NVFP4 weight layout (per expert, per projection; reduction dimension contiguous):
+ *  - codes: uint8, two 4-bit E2M1 codes per byte, the even element in the low nibble
+ *    (E2M1: sign bit 3, 2 exponent bits with bias 1, 1 mantissa bit; magnitudes
+ *    0, 0.5, 1, 1.5, 2, 3, 4, 6);
+ *  - block scales: one E4M3 (fn) byte per 16 consecutive elements of a row;
+ *  - one FP32 tensor scale per expert and projection;
+ *  - element value = e2m1(code) * e4m3(block scale) * tensor scale.
+ *  W13 of expert e is [2I, H]: rows [0, I) are the gate projection, rows [I, 2I) the up
+ *  projection. W2 of expert e is [H, I].
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FT_OK = 0,
+  FT_ERR_INVALID_ARG = 1,       /* null pointer, k < 1, k > E, T < 1, bad limit, ... */
+  FT_ERR_UNSUPPORTED_SHAPE = 2, /* H or I not a multiple of 128, k > 32, E > 4096, ...  */
+  FT_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment stated below          */
+  FT_ERR_WORKSPACE_TOO_SMALL = 4,
+  FT_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed                 */
+  FT_ERR_DEVICE_FLAG = 6,       /* a kernel saw an expert id outside [0, E)             */
+  FT_ERR_TIMEOUT = 7            /* reserved: a bounded device-side wait gave up         */
+} ft_status;
+
+/* Routed experts, all device pointers, 16-byte aligned:
+ *   w13        uint8 [E, 2I, H/2]   w13_scale uint8 [E, 2I, H/16]   w13_gscale float [E]
+ *   w2         uint8 [E, H,  I/2]   w2_scale  uint8 [E, H,  I/16]   w2_gscale  float [E]
+ * (the gscale arrays need only 4-byte alignment). */
+typedef struct {
+  int32_t E, H, I;
+  const uint8_t* w13;
+  const uint8_t* w13_scale;
+  const float* w13_gscale;
+  const uint8_t* w2;
+  const uint8_t* w2_scale;
+  const float* w2_gscale;
+} ft_nvfp4_experts;
+
+/* Optional dense shared expert with the routed experts' H and I (same layouts without
+ * the E dimension; the two gscale pointers point at one device float each) and its gate
+ * vector gv (bf16 [H]). Its output is scaled by sigmoid(x_t . gv) and added to y_t. */
+typedef struct {
+  const uint8_t* w13;
+  const uint8_t* w13_scale;
+  const float* w13_gscale;
+  const uint8_t* w2;
+  const uint8_t* w2_scale;
+  const float* w2_gscale;
+  const uint16_t* gate;
+} ft_nvfp4_shared_expert;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int32_t ft_moe_abi_version(void);
+
+/* Text for a status code (static storage, never NULL). */
+const char* ft_status_string(ft_status s);
+
+/*
+ * ft_moe_route — router softmax -> top-k -> renormalise, one warp per token.
+ *   logits    float [T, E] (4-byte aligned), must be finite
+ *   topk_idx  int32 [T, k] out: the k experts with the largest logits, in descending
+ *             logit order; equal logits go to the lower expert index. Ranking uses the
+ *             fp32 logits themselves, so the choice is exact.
+ *   topk_w    float [T, k] out: softmax over all E renormalised over the kept k, i.e.
+ *             exp(l_j - l_max) / sum over kept i of exp(l_i - l_max).
+ *   1 <= k <= min(E, 32), 1 <= E <= 4096, T >= 1.
+ */
+ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
+                       int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Workspace bytes that decode (prefill = 0) or prefill (prefill = 1) needs for these
+ * sizes; has_shared = 1 when a shared expert is passed. Returns 0 for invalid sizes. */
+size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                              int32_t has_shared, int32_t prefill);
+
+/* Zero a workspace once after allocating it (the error word and the reduction counters
+ * must start at zero; every call leaves them at zero again). Enqueued on `stream`. */
+ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ft_moe_nvfp4_decode — the expert part of the layer for a decode batch (1 <= T <= 64).
+ *   x            bf16 [T, H] (16-byte aligned)
+ *   topk_idx     int32 [T, k], topk_w float [T, k]: as written by ft_moe_route (any
+ *                source is accepted; an id outside [0, E) raises FT_ERR_DEVICE_FLAG in the
+ *                workspace error word and that slot contributes nothing)
+ *   ex           routed experts (see ft_nvfp4_experts); ex->H, ex->I multiples of 128,
+ *                H <= 16384, I <= 8192
+ *   sh           shared expert or NULL
+ *   swiglu_limit L in (0, 128]: h = silu(min(g, L)) * clamp(u, -L, L)
+ *   out          bf16 [T, H] (16-byte aligned), fully overwritten:
+ *                y_t = sum_j topk_w[t,j] * W2_e (h_tj) [+ sigmoid(x_t.gv) * shared(x_t)]
+ *   workspace    device scratch of at least ft_moe_workspace_bytes(T,k,E,H,I,sh!=0,0)
+ *                bytes, 256-byte aligned, zeroed once by ft_moe_workspace_init; calls that
+ *                share a workspace must be ordered on one stream.
+ */
+ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                              const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                              const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                              uint16_t* out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * ft_moe_nvfp4_prefill — the same layer for a multi-token chunk (any T >= 1), run as
+ * grouped dense contractions: tokens are grouped by expert on the GPU, NVFP4 tiles are
+ * dequantised to bf16 on chip and multiplied on the tensor cores. Arguments as for
+ * decode, with workspace of at least ft_moe_workspace_bytes(T,k,E,H,I,sh!=0,1) bytes.
+ */
+ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                               const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                               const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                               uint16_t* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Synchronise `stream`, read the workspace error word, clear it, and return FT_OK or the
+ * first error flagged since the last call (FT_ERR_DEVICE_FLAG, FT_ERR_TIMEOUT). */
+ft_status ft_moe_get_error(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FT_MOE_H */

@@ -1,0 +1,182 @@
+// C ABI of the library: argument checks, workspace sizing and dispatch to the kernels.
+// Every check runs on the host before anything is enqueued.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/ft_moe.h"
+#include "ftmoe_internal.h"
+#include "ftmoe_layout.h"
+
+using namespace ftmoe;
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};  // per-device attribute cache
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ft_status check_experts(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh) {
+  if (!ex) return FT_ERR_INVALID_ARG;
+  if (ex->E < 1 || ex->H < 1 || ex->I < 1) return FT_ERR_INVALID_ARG;
+  if (ex->E > kMaxExperts || ex->H % 128 != 0 || ex->I % 128 != 0 || ex->H > 16384 ||
+      ex->I > 8192)
+    return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!ex->w13 || !ex->w13_scale || !ex->w13_gscale || !ex->w2 || !ex->w2_scale ||
+      !ex->w2_gscale)
+    return FT_ERR_INVALID_ARG;
+  if (!aligned(ex->w13, 16) || !aligned(ex->w13_scale, 16) || !aligned(ex->w2, 16) ||
+      !aligned(ex->w2_scale, 16) || !aligned(ex->w13_gscale, 4) || !aligned(ex->w2_gscale, 4))
+    return FT_ERR_MISALIGNED;
+  if (sh) {
+    if (!sh->w13 || !sh->w13_scale || !sh->w13_gscale || !sh->w2 || !sh->w2_scale ||
+        !sh->w2_gscale || !sh->gate)
+      return FT_ERR_INVALID_ARG;
+    if (!aligned(sh->w13, 16) || !aligned(sh->w13_scale, 16) || !aligned(sh->w2, 16) ||
+        !aligned(sh->w2_scale, 16) || !aligned(sh->w13_gscale, 4) ||
+        !aligned(sh->w2_gscale, 4) || !aligned(sh->gate, 2))
+      return FT_ERR_MISALIGNED;
+  }
+  return FT_OK;
+}
+
+ExpertPtrs to_ptrs(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh) {
+  ExpertPtrs p;
+  p.E = ex->E; p.H = ex->H; p.I = ex->I;
+  p.w13 = ex->w13; p.s13 = ex->w13_scale; p.g13 = ex->w13_gscale;
+  p.w2 = ex->w2; p.s2 = ex->w2_scale; p.g2 = ex->w2_gscale;
+  p.sh_w13 = sh ? sh->w13 : nullptr; p.sh_s13 = sh ? sh->w13_scale : nullptr;
+  p.sh_w2 = sh ? sh->w2 : nullptr; p.sh_s2 = sh ? sh->w2_scale : nullptr;
+  p.sh_g13 = sh ? sh->w13_gscale : nullptr; p.sh_g2 = sh ? sh->w2_gscale : nullptr;
+  p.sh_gate = sh ? sh->gate : nullptr;
+  return p;
+}
+
+ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                           const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                           const ft_nvfp4_shared_expert* sh, float limit, const uint16_t* out,
+                           const void* ws) {
+  ft_status st = check_experts(ex, sh);
+  if (st != FT_OK) return st;
+  if (!x || !topk_idx || !topk_w || !out || !ws) return FT_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!(limit > 0.0f) || !(limit <= 128.0f)) return FT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(ws, 256))
+    return FT_ERR_MISALIGNED;
+  return FT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ft_moe_abi_version(void) { return kAbiVersion; }
+
+const char* ft_status_string(ft_status s) {
+  switch (s) {
+    case FT_OK: return "FT_OK";
+    case FT_ERR_INVALID_ARG: return "FT_ERR_INVALID_ARG: invalid argument";
+    case FT_ERR_UNSUPPORTED_SHAPE: return "FT_ERR_UNSUPPORTED_SHAPE: shape outside the supported range";
+    case FT_ERR_MISALIGNED: return "FT_ERR_MISALIGNED: pointer alignment";
+    case FT_ERR_WORKSPACE_TOO_SMALL: return "FT_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case FT_ERR_CUDA: return "FT_ERR_CUDA: CUDA runtime error";
+    case FT_ERR_DEVICE_FLAG: return "FT_ERR_DEVICE_FLAG: expert id outside [0, E) or repeated in a token";
+    case FT_ERR_TIMEOUT: return "FT_ERR_TIMEOUT: bounded device wait expired";
+  }
+  return "unknown ft_status";
+}
+
+ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
+                       int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!logits || !topk_idx || !topk_w) return FT_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || k < 1 || k > E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK || E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+    return FT_ERR_MISALIGNED;
+  cudaError_t err = launch_route(logits, T, E, k, topk_idx, topk_w,
+                                 static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                              int32_t has_shared, int32_t prefill) {
+  if (T < 1 || k < 1 || E < 1 || H < 1 || I < 1 || k > E) return 0;
+  if (!prefill) {
+    if (T > kMaxDecodeT) return 0;
+    return DecodeLayout(T, k, E, H, I, has_shared != 0).total;
+  }
+  return 0;  // prefill workspace: see ft_moe_nvfp4_prefill
+}
+
+ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return FT_ERR_INVALID_ARG;
+  cudaError_t err =
+      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                              const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                              const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                              uint16_t* out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  ft_status st =
+      check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
+  if (st != FT_OK) return st;
+  if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
+  const DecodeLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr);
+  if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return FT_ERR_CUDA;
+  cudaError_t err = launch_decode(x, T, topk_idx, topk_w, k, to_ptrs(ex, sh), swiglu_limit, out,
+                                  workspace, sms, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                               const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                               const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                               uint16_t* out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  ft_status st =
+      check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
+  if (st != FT_OK) return st;
+  (void)workspace_bytes;
+  (void)stream;
+  return FT_ERR_UNSUPPORTED_SHAPE;
+}
+
+ft_status ft_moe_get_error(void* workspace, void* stream) {
+  if (!workspace) return FT_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FT_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FT_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FT_ERR_CUDA;
+  }
+  if (word & kErrBadExpert) return FT_ERR_DEVICE_FLAG;
+  if (word & kErrTimeout) return FT_ERR_TIMEOUT;
+  return FT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+"""Helpers for the GPU tests: move a synthetic layer to the device, run the library,
+and score a bf16 result against the oracle's float32 output."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Acceptance bound for the bf16 layer output against the float32 oracle (whole [T, H]
+# output, fp64 arithmetic): relative Frobenius error <= 5e-3 and max |err| <= 2e-2 * rms.
+REL_FRO_TOL = 5e-3
+MAX_ABS_RMS_TOL = 2e-2
+
+
+def ftmoe():
+    from nvfp4_mixture_experts_02_gb300 import ftmoe as m   # raises if the .so is missing
+    return m
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def experts_to_device(layer, device="cuda"):
+    m = ftmoe()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    ex = m.NvFP4Experts(t(layer.w13), t(layer.s13), t(layer.g13), t(layer.w2), t(layer.s2),
+                        t(layer.g2))
+    sh = None
+    if layer.shared is not None:
+        s = layer.shared
+        sh = m.NvFP4Shared(t(s["w13"]), t(s["s13"]), t(np.array([s["g13"]], np.float32)),
+                           t(s["w2"]), t(s["s2"]), t(np.array([s["g2"]], np.float32)),
+                           bf16_tensor(s["gate"], device))
+    return ex, sh
+
+
+def score(y_gpu: np.ndarray, y_ref: np.ndarray):
+    """(relative Frobenius error, max |err| / rms(ref)) in fp64."""
+    y_gpu = np.asarray(y_gpu, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    diff = y_gpu - y_ref
+    fro = np.linalg.norm(diff) / max(np.linalg.norm(y_ref), 1e-300)
+    rms = np.sqrt(np.mean(y_ref ** 2))
+    return fro, np.max(np.abs(diff)) / max(rms, 1e-300)
+
+
+def assert_close(y_gpu, y_ref, what=""):
+    fro, mx = score(y_gpu, y_ref)
+    assert np.all(np.isfinite(y_gpu)), f"{what}: non-finite output"
+    assert fro <= REL_FRO_TOL and mx <= MAX_ABS_RMS_TOL, \
+        f"{what}: rel_fro={fro:.3e} (<= {REL_FRO_TOL}), max_abs/rms={mx:.3e} (<= {MAX_ABS_RMS_TOL})"
+    return fro, mx

@@ -1,0 +1,102 @@
+"""The C-ABI library on the CPU: it loads, exports every function include/ft_moe.h
+declares, and rejects invalid arguments on the host before touching the GPU (the fake
+pointers below are never dereferenced: every call fails validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "ft_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_mixture_experts_02_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from nvfp4_mixture_experts_02_gb300 import ftmoe
+    return ftmoe
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ft_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("ft_moe_route", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(so, name), f"{name} declared in ft_moe.h but not exported"
+    assert set(declared_functions()) == set(lib.EXPORTED)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.abi_version() == 1
+    for st in range(8):
+        assert lib.status_string(st).startswith(lib.STATUS_NAMES[st])
+
+
+def test_workspace_bytes(lib):
+    small = lib.workspace_bytes(1, 2, 8, 256, 128, False)
+    assert small > 0 and small % 256 == 0
+    assert lib.workspace_bytes(1, 10, 512, 4096, 1024, True) > small
+    assert lib.workspace_bytes(65, 10, 512, 4096, 1024, True) == 0     # decode limit T<=64
+    assert lib.workspace_bytes(1, 9, 8, 256, 128, False) == 0          # k > E
+
+
+def _experts(lib, E=8, H=256, I=128, base=0x10000, **over):
+    p = dict(w13=base, w13_scale=base + 0x1000, w13_gscale=base + 0x2000, w2=base + 0x3000,
+             w2_scale=base + 0x4000, w2_gscale=base + 0x5000)
+    p.update(over)
+    return lib._Experts(E, H, I, p["w13"], p["w13_scale"], p["w13_gscale"], p["w2"],
+                        p["w2_scale"], p["w2_gscale"])
+
+
+def _decode(lib, ex, T=1, k=2, x=0x20000, idx=0x30000, w=0x40000, out=0x50000, ws=0x60000,
+            limit=7.0, ws_bytes=1 << 30):
+    return lib.lib().ft_moe_nvfp4_decode(x, T, idx, w, k, ctypes.byref(ex), None, limit, out,
+                                         ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(ex=dict(w13=0)), 1),                       # null weight pointer
+    (dict(ex=dict(H=200)), 2),                       # H not a multiple of 128
+    (dict(ex=dict(I=96)), 2),                        # I not a multiple of 128
+    (dict(ex=dict(E=5000)), 2),                      # too many experts
+    (dict(ex=dict(w2=0x10008)), 3),                  # misaligned weight pointer
+    (dict(call=dict(k=9)), 1),                       # k > E
+    (dict(call=dict(k=0)), 1),
+    (dict(call=dict(T=0)), 1),
+    (dict(call=dict(T=65)), 2),                      # decode batch limit
+    (dict(call=dict(limit=0.0)), 1),
+    (dict(call=dict(limit=float("nan"))), 1),
+    (dict(call=dict(limit=1000.0)), 1),
+    (dict(call=dict(x=0x20002)), 3),                 # misaligned activations
+    (dict(call=dict(ws=0x60010)), 3),                # workspace not 256-byte aligned
+    (dict(call=dict(ws_bytes=16)), 4),               # workspace too small
+    (dict(call=dict(out=0)), 1),
+])
+def test_decode_rejects_invalid_arguments(lib, case, expect):
+    exargs = dict(case.get("ex", {}))
+    dims = {k_: exargs.pop(k_) for k_ in ("E", "H", "I") if k_ in exargs}
+    ex = _experts(lib, **dims, **exargs)
+    assert _decode(lib, ex, **case.get("call", {})) == expect
+
+
+def test_route_rejects_invalid_arguments(lib):
+    f = lib.lib().ft_moe_route
+    assert f(0, 1, 8, 2, 0x1000, 0x2000, None) == 1          # null logits
+    assert f(0x1000, 1, 8, 9, 0x1000, 0x2000, None) == 1     # k > E
+    assert f(0x1000, 1, 64, 33, 0x1000, 0x2000, None) == 2   # k > 32
+    assert f(0x1002, 1, 8, 2, 0x1000, 0x2000, None) == 3     # misaligned
+    assert f(0x1000, 0, 8, 2, 0x1000, 0x2000, None) == 1     # T = 0
