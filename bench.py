@@ -248,12 +248,15 @@ def run_ours(args, spec, rank, world, local):
         achieved = flops_call / (dec_us * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
                 "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": None,
-                "peak_source": src, "kernel": "ft_moe_nvfp4_prefill"}
+                "peak_source": src, "us_per_launch": round(dec_us, 3),
+                "kernel": "ft_moe_nvfp4_prefill (plan, activations, W13 and W2 tcgen05 "
+                          "grouped GEMMs, reduce)",
+                "hbm_bound_frac": round((bytes_call / (hbm * 1e9)) / (dec_us * 1e-6), 4)}
     else:
         achieved = bytes_call / (dec_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
-                "kernel": "ft_moe_nvfp4_decode (plan + W13/SwiGLU + W2/sum kernels)",
+                "kernel": "k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in one launch)",
                 "us_per_launch": round(dec_us, 3)}
     res = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
@@ -269,7 +272,7 @@ def run_ours(args, spec, rank, world, local):
                    "graph": "CUDA graph of one pass over the instances",
                    "bytes_per_call": round(bytes_call), "experts_touched_mean":
                    statistics.mean(touched)},
-        "roofline": roof, "e2e": e2e, "gpu_launches": 4 * steps_done,
+        "roofline": roof, "e2e": e2e, "gpu_launches": (6 if prefill else 2) * steps_done,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

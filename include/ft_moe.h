@@ -69,7 +69,7 @@ typedef struct {
 
 /* Optional dense shared expert with the routed experts' H and I (same layouts without
  * the E dimension; the two gscale pointers point at one device float each) and its gate
- * vector gv (bf16 [H]). Its output is scaled by sigmoid(x_t . gv) and added to y_t. */
+ * vector gv (bf16 [H], 16-byte aligned). Its output is scaled by sigmoid(x_t . gv) and added to y_t. */
 typedef struct {
   const uint8_t* w13;
   const uint8_t* w13_scale;
@@ -100,7 +100,9 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                        int32_t* topk_idx, float* topk_w, void* stream);
 
 /* Workspace bytes that decode (prefill = 0) or prefill (prefill = 1) needs for these
- * sizes; has_shared = 1 when a shared expert is passed. Returns 0 for invalid sizes. */
+ * sizes on the current device; has_shared = 1 when a shared expert is passed. Without a
+ * usable device the decode figure is an upper bound for any GPU. Returns 0 for invalid
+ * sizes. */
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                               int32_t has_shared, int32_t prefill);
 
@@ -141,6 +143,10 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
                                const ft_nvfp4_shared_expert* sh, float swiglu_limit,
                                uint16_t* out, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/* Text of the last CUDA runtime error seen by this thread inside the library (the cause
+ * behind an FT_ERR_CUDA); static storage, never NULL. */
+const char* ft_moe_last_cuda_error(void);
 
 /* Synchronise `stream`, read the workspace error word, clear it, and return FT_OK or the
  * first error flagged since the last call (FT_ERR_DEVICE_FLAG, FT_ERR_TIMEOUT). */

@@ -28,6 +28,14 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+ft_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FT_OK;
+  t_last_cuda = e;
+  return FT_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 ft_status check_experts(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh) {
@@ -48,7 +56,7 @@ ft_status check_experts(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert
       return FT_ERR_INVALID_ARG;
     if (!aligned(sh->w13, 16) || !aligned(sh->w13_scale, 16) || !aligned(sh->w2, 16) ||
         !aligned(sh->w2_scale, 16) || !aligned(sh->w13_gscale, 4) ||
-        !aligned(sh->w2_gscale, 4) || !aligned(sh->gate, 2))
+        !aligned(sh->w2_gscale, 4) || !aligned(sh->gate, 16))
       return FT_ERR_MISALIGNED;
   }
   return FT_OK;
@@ -109,9 +117,8 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
   if (k > kMaxTopK || E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
     return FT_ERR_MISALIGNED;
-  cudaError_t err = launch_route(logits, T, E, k, topk_idx, topk_w,
-                                 static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+  return cuda_status(launch_route(logits, T, E, k, topk_idx, topk_w,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
@@ -119,16 +126,17 @@ size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_
   if (T < 1 || k < 1 || E < 1 || H < 1 || I < 1 || k > E) return 0;
   if (!prefill) {
     if (T > kMaxDecodeT) return 0;
-    return DecodeLayout(T, k, E, H, I, has_shared != 0).total;
+    const int sms = sm_count();   // grid of the decode kernel on the current device
+    return DecodeLayout(T, k, E, H, I, has_shared != 0, sms > 0 && sms < kMaxGrid ? sms : kMaxGrid)
+        .total;
   }
-  return 0;  // prefill workspace: see ft_moe_nvfp4_prefill
+  return PrefillLayout(T, k, E, H, I, has_shared != 0).total;
 }
 
 ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes == 0) return FT_ERR_INVALID_ARG;
-  cudaError_t err =
-      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+  return cuda_status(
+      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_idx,
@@ -140,13 +148,15 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
       check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
   if (st != FT_OK) return st;
   if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
-  const DecodeLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr);
-  if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
+  // smallest possible workspace first (no CUDA call), then the exact one for this device
+  if (workspace_bytes < DecodeLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr, 1).total)
+    return FT_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count();
   if (sms <= 0) return FT_ERR_CUDA;
-  cudaError_t err = launch_decode(x, T, topk_idx, topk_w, k, to_ptrs(ex, sh), swiglu_limit, out,
-                                  workspace, sms, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+  const DecodeLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr, sms < kMaxGrid ? sms : kMaxGrid);
+  if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_decode(x, T, topk_idx, topk_w, k, to_ptrs(ex, sh), swiglu_limit,
+                                   out, workspace, sms, static_cast<cudaStream_t>(stream)));
 }
 
 ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk_idx,
@@ -157,22 +167,30 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
   ft_status st =
       check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
   if (st != FT_OK) return st;
-  (void)workspace_bytes;
-  (void)stream;
-  return FT_ERR_UNSUPPORTED_SHAPE;
+  const PrefillLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr);
+  if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return FT_ERR_CUDA;
+  return cuda_status(launch_prefill(x, T, topk_idx, topk_w, k, to_ptrs(ex, sh), swiglu_limit,
+                                    out, workspace, sms, static_cast<cudaStream_t>(stream)));
+}
+
+const char* ft_moe_last_cuda_error(void) {
+  return t_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda);
 }
 
 ft_status ft_moe_get_error(void* workspace, void* stream) {
   if (!workspace) return FT_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return FT_ERR_CUDA;
+  ft_status st = cuda_status(cudaStreamSynchronize(s));
+  if (st != FT_OK) return st;
   int word = 0;
-  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return FT_ERR_CUDA;
+  st = cuda_status(cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost));
+  if (st != FT_OK) return st;
   if (word != 0) {
     const int zero = 0;
-    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
-      return FT_ERR_CUDA;
+    st = cuda_status(cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice));
+    if (st != FT_OK) return st;
   }
   if (word & kErrBadExpert) return FT_ERR_DEVICE_FLAG;
   if (word & kErrTimeout) return FT_ERR_TIMEOUT;

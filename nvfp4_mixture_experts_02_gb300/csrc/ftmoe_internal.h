@@ -27,4 +27,17 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
                           int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
                           int num_sms, cudaStream_t stream);
 
+// Workspace regions of the prefill path (byte offsets, 256-byte aligned).
+struct PrefillLayout {
+  int max_pairs = 0, max_groups = 0;
+  size_t err = 0, hdr = 0, act_expert = 0, act_pair0 = 0, group_act = 0, group_p0 = 0,
+         group_n = 0, pair_tok = 0, pair_w = 0, pair_slot = 0, xf = 0, xscale = 0, h = 0,
+         part = 0, total = 0;
+  PrefillLayout(int T, int k, int E, int H, int I, bool shared);
+};
+
+cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
+                           int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
+                           int num_sms, cudaStream_t stream);
+
 }  // namespace ftmoe

@@ -1,0 +1,643 @@
+// Prefill path of the NVFP4 MoE layer (any T): the expert products run as grouped dense
+// contractions on the 5th-generation tensor cores (tcgen05), which is where a
+// multi-token chunk has enough reuse per weight to need them.
+//
+//   k_pf_plan    (1 CTA)    group the (token, slot) pairs by expert; token groups of at
+//                           most 128 per expert; pair weights; per-token slot -> pair map
+//   k_pf_act     (T warps)  f16 activations with a per-token power-of-two scale, and the
+//                           shared-expert gate
+//   k_pf_gemm<W13>          h[pair, I] = SwiGLU(G x, U x) * pair weight (f16)
+//   k_pf_gemm<W2>           part[pair, H] = W2 h (fp32), per pair
+//   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
+//                           part[pair], in slot order (deterministic), bf16 out
+//
+// k_pf_gemm is persistent (one CTA per SM, 8 warps). A work item is one token group of
+// one expert (up to 128 tokens, the MMA N) against 256 weight rows: for W13 the 128 gate
+// rows and the 128 matching up rows of a row block (two fp32 accumulators in tensor
+// memory, so SwiGLU pairs land in the same TMEM lane), for W2 two 128-row blocks of the
+// output. Each thread owns one weight row: it streams the row's packed E2M1 codes and E4M3
+// scales with 16-byte loads (4 chunks in flight), forms e2m1*e4m3 exactly in f16
+// (hardware conversions + one f16x2 multiply per pair) and writes it into tensor memory
+// (tcgen05.st) as the MMA's A operand. The activations of the group (B operand) are
+// gathered into shared memory in the canonical K-major core-matrix layout. One thread
+// issues tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group
+// size rounded up to 16, K=16 per instruction) and commits to an mbarrier per stage; two
+// stages let the dequantisation of chunk c+1 overlap the MMAs of chunk c.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ftmoe_internal.h"
+#include "ftmoe_tc.cuh"
+
+namespace ftmoe {
+
+namespace {
+
+constexpr int kPfThreads = 256;          // 8 warps: rows 0-127 of set 0 / set 1
+constexpr int kPfN = 128;                // max tokens per group (MMA N)
+constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
+constexpr int kPfStages = 2;
+constexpr int kPfDepth = 4;              // chunks of codes in flight per thread
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 x 32 columns
+constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 16 KB per stage
+
+struct PfPlanArgs {
+  const int* topk_idx;
+  const float* topk_w;
+  int T, k, E;
+  const float* g2;
+  const float* sh_g2;   // null: no shared expert
+  float hscale;
+  int* err;
+  // outputs
+  int* hdr;             // [0] n_act [1] n_groups [2] n_pairs [3] g2ref bits [4] n_routed
+  int* act_expert;      // [E+1]
+  int* act_pair0;       // [E+2]
+  int* group_act;       // [max_groups]
+  int* group_p0;
+  int* group_n;
+  int* pair_tok;        // [P]
+  float* pair_w;        // [P]
+  int* pair_slot;       // [T*k]: pair of (token, slot), -1 if the slot was invalid
+  int max_groups;
+};
+
+// The grouping runs in one CTA; pair positions inside an expert come from shared-memory
+// atomics (their order is not reproducible, but every pair's value is computed from its
+// own token only and the final sum runs in slot order, so the output bits are).
+__global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
+  __shared__ int cnt[kMaxExperts + 1];       // pair counts, then fill counters
+  __shared__ int act_of_e[kMaxExperts + 1];
+  __shared__ float red[32];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int T = p.T, k = p.k, E = p.E, TK = T * k;
+  const bool has_shared = p.sh_g2 != nullptr;
+  for (int e = tid; e <= E; e += nthr) cnt[e] = 0;
+  __syncthreads();
+  for (int q = tid; q < TK; q += nthr) {
+    const int t = q / k, j = q - t * k;
+    const int e = p.topk_idx[q];
+    bool ok = e >= 0 && e < E;
+    for (int jj = 0; jj < j && ok; ++jj) ok = p.topk_idx[t * k + jj] != e;
+    if (ok) atomicAdd(&cnt[e], 1);
+    else atomicOr(p.err, kErrBadExpert);
+  }
+  __syncthreads();
+  // active experts in ascending id order (serial scan by warp 0: E <= 4096)
+  if (warp == 0) {
+    int base_a = 0, base_p = 0, base_g = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? cnt[e] : 0;
+      const int f = c > 0;
+      const int ng = (c + kPfN - 1) / kPfN;
+      int ia = f, ip = c, ig = ng;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int va = __shfl_up_sync(0xffffffffu, ia, o);
+        const int vp = __shfl_up_sync(0xffffffffu, ip, o);
+        const int vg = __shfl_up_sync(0xffffffffu, ig, o);
+        if (lane >= o) {
+          ia += va;
+          ip += vp;
+          ig += vg;
+        }
+      }
+      if (f) {
+        const int a = base_a + ia - 1, p0 = base_p + ip - c, g0 = base_g + ig - ng;
+        act_of_e[e] = a;
+        p.act_expert[a] = e;
+        p.act_pair0[a] = p0;
+        for (int g = 0; g < ng; ++g) {
+          p.group_act[g0 + g] = a;
+          p.group_p0[g0 + g] = p0 + g * kPfN;
+          p.group_n[g0 + g] = min(kPfN, c - g * kPfN);
+        }
+      } else if (e < E) {
+        act_of_e[e] = -1;
+      }
+      base_a += __shfl_sync(0xffffffffu, ia, 31);
+      base_p += __shfl_sync(0xffffffffu, ip, 31);
+      base_g += __shfl_sync(0xffffffffu, ig, 31);
+    }
+    if (lane == 0) {
+      int n_act = base_a, n_pairs = base_p, n_groups = base_g;
+      p.act_pair0[n_act] = n_pairs;
+      p.hdr[4] = n_act;
+      if (has_shared) {
+        p.act_expert[n_act] = -1;
+        const int ng = (T + kPfN - 1) / kPfN;
+        for (int g = 0; g < ng; ++g) {
+          p.group_act[n_groups + g] = n_act;
+          p.group_p0[n_groups + g] = n_pairs + g * kPfN;
+          p.group_n[n_groups + g] = min(kPfN, T - g * kPfN);
+        }
+        n_groups += ng;
+        n_pairs += T;
+        n_act += 1;
+        p.act_pair0[n_act] = n_pairs;
+      }
+      p.hdr[0] = n_act;
+      p.hdr[1] = n_groups;
+      p.hdr[2] = n_pairs;
+    }
+  }
+  __syncthreads();
+  const int n_routed = p.hdr[4];
+  // reference W2 tensor scale
+  float gmax = 0.f;
+  for (int i = tid; i < n_routed; i += nthr) gmax = fmaxf(gmax, p.g2[p.act_expert[i]]);
+  if (tid == 0 && has_shared) gmax = fmaxf(gmax, *p.sh_g2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+  if (lane == 0) red[warp] = gmax;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < (nthr >> 5) ? red[tid] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (tid == 0) {
+      red[0] = v > 0.f ? v : 1.f;
+      p.hdr[3] = __float_as_int(red[0]);
+    }
+  }
+  __syncthreads();
+  const float g2ref = red[0];
+  int* fill = cnt;   // counts are no longer needed: reuse them as fill counters
+  for (int e = tid; e <= E; e += nthr) fill[e] = 0;
+  __syncthreads();
+  // place the pairs
+  for (int q = tid; q < TK; q += nthr) {
+    const int t = q / k, j = q - t * k;
+    const int e = p.topk_idx[q];
+    bool ok = e >= 0 && e < E;
+    for (int jj = 0; jj < j && ok; ++jj) ok = p.topk_idx[t * k + jj] != e;
+    if (!ok) {
+      p.pair_slot[q] = -1;
+      continue;
+    }
+    const int a = act_of_e[e];
+    const int pos = p.act_pair0[a] + atomicAdd(&fill[e], 1);
+    p.pair_tok[pos] = t;
+    p.pair_w[pos] = p.topk_w[q] * (p.g2[e] / g2ref) * p.hscale;
+    p.pair_slot[q] = pos;
+  }
+  if (has_shared) {
+    const int pr0 = p.act_pair0[n_routed];
+    for (int t = tid; t < T; t += nthr) p.pair_tok[pr0 + t] = t;
+  }
+}
+
+struct PfActArgs {
+  const uint16_t* x;
+  int T, H;
+  const uint16_t* sh_gate;
+  const float* sh_g2;
+  float hscale;
+  const int* hdr;
+  const int* act_pair0;
+  float* pair_w;
+  __half* xf;
+  float* xscale;
+};
+
+// One warp per token: f16 copy of x scaled so that max |x| is in [2^14, 2^15), and the
+// shared expert's weight sigmoid(x . gv) * (W2 scale ratio) * 2^S.
+__global__ void __launch_bounds__(256) k_pf_act(const PfActArgs p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= p.T) return;
+  const uint16_t* xr = p.x + (size_t)t * p.H;
+  float amax = 0.f, dot = 0.f;
+  for (int c = lane * 8; c < p.H; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 gv = make_uint4(0, 0, 0, 0);
+    if (p.sh_gate) gv = *reinterpret_cast<const uint4*>(p.sh_gate + c);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+      dot = fmaf(lo, __uint_as_float(gw[j] << 16), dot);
+      dot = fmaf(hi, __uint_as_float(gw[j] & 0xFFFF0000u), dot);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  dot = __shfl_sync(0xffffffffu, dot, 0);
+  int ex = 0;
+  if (amax > 0.f) {
+    frexpf(amax, &ex);
+    ex -= 15;
+  }
+  const float down = ldexpf(1.f, -ex);
+  __half* dst = p.xf + (size_t)t * p.H;
+  for (int c = lane * 8; c < p.H; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * down,
+                                           __uint_as_float(w[j] & 0xFFFF0000u) * down);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(dst + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) {
+    p.xscale[t] = ldexpf(1.f, ex);
+    if (p.sh_gate) {
+      const float g2ref = __int_as_float(p.hdr[3]);
+      const int pr = p.act_pair0[p.hdr[4]] + t;
+      p.pair_w[pr] = 1.f / (1.f + expf(-dot)) * (*p.sh_g2 / g2ref) * p.hscale;
+    }
+  }
+}
+
+struct PfGemmArgs {
+  // weights of the two row sets: W13 -> gate / up rows; W2 -> output rows
+  const uint8_t *w, *s, *sh_w, *sh_s;
+  int H, I, T;
+  const int* hdr;
+  const int* act_expert;
+  const int* group_act;
+  const int* group_p0;
+  const int* group_n;
+  const int* pair_tok;
+  const float* pair_w;
+  const float* act_g13;   // unused for W2
+  const float* g13;       // routed W13 tensor scales
+  const float* sh_g13;
+  const __half* b_src;    // W13: f16 activations [T, H]; W2: h [P, I]
+  const float* xscale;
+  __half* h_out;          // W13 output
+  float* part_out;        // W2 output (fp32 per pair)
+  float limit, oscale_mul;  // W2: output scale = g2ref * oscale_mul (= 1 / 2^S)
+  int* err;
+};
+
+template <bool kW13>
+__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant__ PfGemmArgs p) {
+  extern __shared__ __align__(1024) unsigned char pf_smem[];
+  __shared__ __align__(8) uint64_t mbar[kPfStages];
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int s_tok[kPfN];
+  __shared__ float s_w[kPfN];
+  __shared__ float s_xs[kPfN];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int set = warp >> 2;                 // row set 0 / 1
+  const int m = (warp & 3) * 32 + lane;      // row inside the set = TMEM lane
+  unsigned char* sB = pf_smem;               // [kPfStages][kBTileBytes]
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) mbar_init(&mbar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_slot;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+
+  griddep_launch_dependents();
+  griddep_wait();
+
+  const int n_groups = p.hdr[1];
+  const int K = kW13 ? p.H : p.I;
+  const int nchunks = K / kPfKc;
+  const int blocks = kW13 ? p.I / 128 : p.H / 256;
+  const int n_items = n_groups * blocks;
+  const size_t rowb = (size_t)K / 2, srowb = (size_t)K / 16;
+  uint32_t uses[kPfStages] = {0, 0};   // completed-use count per stage (phase parity)
+  bool ok = true;
+
+  for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    const int gi = item / blocks, rb = item - gi * blocks;
+    const int a = p.group_act[gi];
+    const int e = p.act_expert[a];
+    const int p0 = p.group_p0[gi], nv = p.group_n[gi];
+    const int npad = (nv + 15) & ~15;
+    // this thread's weight row
+    int row;
+    if (kW13) row = (set == 0 ? 0 : p.I) + rb * 128 + m;
+    else row = rb * 256 + set * 128 + m;
+    const size_t nrows = kW13 ? 2 * (size_t)p.I : (size_t)p.H;
+    const uint8_t* wrow = (e >= 0 ? p.w + (size_t)e * nrows * rowb : p.sh_w) + (size_t)row * rowb;
+    const uint8_t* srow = (e >= 0 ? p.s + (size_t)e * nrows * srowb : p.sh_s) + (size_t)row * srowb;
+    if (tid < kPfN) {
+      const int n = tid;
+      s_tok[n] = n < nv ? p.pair_tok[p0 + n] : 0;
+      if (kW13) {
+        s_w[n] = n < nv ? p.pair_w[p0 + n] : 0.f;
+        s_xs[n] = n < nv ? p.xscale[s_tok[n]] : 0.f;
+      }
+    }
+    __syncthreads();
+
+    // register pipeline of packed codes + scales
+    uint4 q[kPfDepth][2];
+    uint32_t sc[kPfDepth];
+#pragma unroll
+    for (int d = 0; d < kPfDepth; ++d) {
+      if (d < nchunks) {
+        q[d][0] = ldg_stream16(wrow + (size_t)d * 32);
+        q[d][1] = ldg_stream16(wrow + (size_t)d * 32 + 16);
+        sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)d * 4));
+      }
+    }
+    for (int c0 = 0; c0 < nchunks && ok; c0 += kPfDepth) {
+#pragma unroll
+      for (int d = 0; d < kPfDepth; ++d) {
+        const int c = c0 + d;
+        if (c < nchunks && ok) {
+          const int st = c & (kPfStages - 1);
+          // the MMAs that last read this stage's buffers must be done
+          if (uses[st] > 0 || c >= kPfStages) {
+            if (c >= kPfStages || uses[st] > 0) {
+              ok = mbar_wait(&mbar[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
+            }
+          }
+          tc_fence_after();
+          // A: dequantise this row's 64 elements into TMEM
+          uint32_t r[32];
+          dequant64(q[d][0], q[d][1], sc[d], r);
+          const int nx = c + kPfDepth;
+          if (nx < nchunks) {
+            q[d][0] = ldg_stream16(wrow + (size_t)nx * 32);
+            q[d][1] = ldg_stream16(wrow + (size_t)nx * 32 + 16);
+            sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)nx * 4));
+          }
+          tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
+          // B: the group's activations for this chunk, K-major core-matrix layout
+          unsigned char* bt = sB + st * kBTileBytes;
+          for (int i = tid; i < npad * 8; i += kPfThreads) {
+            const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (n < nv) {
+              const size_t src_row = kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n);
+              v = *reinterpret_cast<const uint4*>(p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j);
+            }
+            *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = v;
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_f16(128, npad);
+            const uint32_t b0 = smem_addr(bt);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              const uint32_t dcol = s == 0 ? kColD0 : kColD1;
+#pragma unroll
+              for (int ks = 0; ks < kPfKc / 16; ++ks) {
+                mma_ts(tbase + dcol, tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
+                       smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&mbar[st]);
+          }
+          ++uses[st];
+        }
+      }
+    }
+    // all MMAs of this item done -> read the accumulators
+    if (ok) {
+      for (int st = 0; st < kPfStages; ++st) {
+        // the last use of each stage that was issued
+        if (uses[st] > 0) ok = ok && mbar_wait(&mbar[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
+      }
+    }
+    tc_fence_after();
+    if (ok) {
+      if (kW13) {
+        // warps 0-3 and 4-7 share the lanes; split the columns in blocks of 16
+        const float g13 = e >= 0 ? __ldg(p.g13 + e) : __ldg(p.sh_g13);
+        const int i_out = rb * 128 + m;
+        for (int nb = set * 16; nb < npad; nb += 32) {
+          uint32_t gv[16], uv[16];
+          tmem_ld16(tbase + lane_off + kColD0 + nb, gv);
+          tmem_ld16(tbase + lane_off + kColD1 + nb, uv);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = nb + j;
+            if (n < nv) {
+              const float sc2 = g13 * s_xs[n];
+              const float hv = silu_clamped_swiglu(__uint_as_float(gv[j]) * sc2,
+                                                   __uint_as_float(uv[j]) * sc2, p.limit);
+              p.h_out[(size_t)(p0 + n) * p.I + i_out] = __float2half_rn(hv * s_w[n]);
+            }
+          }
+        }
+      } else {
+        const float oscale = __int_as_float(p.hdr[3]) * p.oscale_mul;
+        const int r_out = rb * 256 + set * 128 + m;
+        const uint32_t dcol = set == 0 ? kColD0 : kColD1;
+        for (int nb = 0; nb < npad; nb += 16) {
+          uint32_t dv[16];
+          tmem_ld16(tbase + lane_off + dcol + nb, dv);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = nb + j;
+            if (n < nv) {
+              p.part_out[(size_t)(p0 + n) * p.H + r_out] = __uint_as_float(dv[j]) * oscale;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();   // accumulators read before the next item's first MMA
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols)
+                 : "memory");
+}
+
+struct PfReduceArgs {
+  const float* part;      // [P, H] fp32
+  const int* pair_slot;   // [T*k]
+  const int* hdr;
+  const int* act_pair0;
+  int T, k, H, has_shared;
+  uint16_t* out;
+};
+
+// y[t, c] = sum over the token's slots in order (then the shared expert) of part[pair, c].
+__global__ void __launch_bounds__(256) k_pf_reduce(const PfReduceArgs p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int per_row = p.H / 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)p.T * per_row) return;
+  const int t = (int)(i / per_row), c8 = (int)(i - (long long)t * per_row) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  auto add = [&](int pr) {
+    const float4* src = reinterpret_cast<const float4*>(p.part + (size_t)pr * p.H + c8);
+    const float4 a = __ldcg(src), b = __ldcg(src + 1);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  };
+  for (int j = 0; j < p.k; ++j) {
+    const int pr = p.pair_slot[t * p.k + j];
+    if (pr >= 0) add(pr);
+  }
+  if (p.has_shared) add(p.act_pair0[p.hdr[4]] + t);
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+    o[j] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(p.out + (size_t)t * p.H + c8) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+cudaLaunchConfig_t pdl_cfg(dim3 g, dim3 b, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = g;
+  cfg.blockDim = b;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+PrefillLayout::PrefillLayout(int T, int k, int E, int H, int I, bool shared) {
+  max_pairs = T * k + (shared ? T : 0);
+  const int routed = T * k < E ? T * k : E;
+  max_groups = (T * k + kPfN - 1) / kPfN + routed + (shared ? (T + kPfN - 1) / kPfN : 0);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  err = take(16);
+  hdr = take(64);
+  act_expert = take(4 * (size_t)(E + 2));
+  act_pair0 = take(4 * (size_t)(E + 3));
+  group_act = take(4 * (size_t)max_groups);
+  group_p0 = take(4 * (size_t)max_groups);
+  group_n = take(4 * (size_t)max_groups);
+  pair_tok = take(4 * (size_t)max_pairs);
+  pair_w = take(4 * (size_t)max_pairs);
+  pair_slot = take(4 * (size_t)T * k);
+  xf = take(2 * (size_t)T * H);
+  xscale = take(4 * (size_t)T);
+  h = take(2 * (size_t)max_pairs * I);
+  part = take(4 * (size_t)max_pairs * H);
+  total = o;
+}
+
+cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
+                           int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
+                           int num_sms, cudaStream_t stream) {
+  const bool shared = ex.sh_w13 != nullptr;
+  const PrefillLayout L(T, k, ex.E, ex.H, ex.I, shared);
+  char* base = static_cast<char*>(ws);
+  auto I32 = [&](size_t off) { return reinterpret_cast<int*>(base + off); };
+  auto F32 = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+  int S = 0;
+  while (S < 24 && (double)limit * limit * std::ldexp(1.0, S + 1) < 65504.0) ++S;
+  const float hscale = (float)std::ldexp(1.0, S);
+  cudaError_t err;
+
+  PfPlanArgs pa;
+  pa.topk_idx = topk_idx; pa.topk_w = topk_w; pa.T = T; pa.k = k; pa.E = ex.E; pa.g2 = ex.g2;
+  pa.sh_g2 = shared ? ex.sh_g2 : nullptr; pa.hscale = hscale; pa.err = I32(L.err);
+  pa.hdr = I32(L.hdr); pa.act_expert = I32(L.act_expert); pa.act_pair0 = I32(L.act_pair0);
+  pa.group_act = I32(L.group_act); pa.group_p0 = I32(L.group_p0); pa.group_n = I32(L.group_n);
+  pa.pair_tok = I32(L.pair_tok); pa.pair_w = F32(L.pair_w); pa.pair_slot = I32(L.pair_slot);
+  pa.max_groups = L.max_groups;
+  {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3(1), dim3(1024), 0, stream, at);
+    if ((err = cudaLaunchKernelEx(&cfg, k_pf_plan, pa)) != cudaSuccess) return err;
+  }
+  PfActArgs aa;
+  aa.x = x; aa.T = T; aa.H = ex.H; aa.sh_gate = shared ? ex.sh_gate : nullptr;
+  aa.sh_g2 = shared ? ex.sh_g2 : nullptr; aa.hscale = hscale; aa.hdr = I32(L.hdr);
+  aa.act_pair0 = I32(L.act_pair0); aa.pair_w = F32(L.pair_w);
+  aa.xf = reinterpret_cast<__half*>(base + L.xf); aa.xscale = F32(L.xscale);
+  {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3((T + 7) / 8), dim3(256), 0, stream, at);
+    if ((err = cudaLaunchKernelEx(&cfg, k_pf_act, aa)) != cudaSuccess) return err;
+  }
+  const size_t smem = (size_t)kPfStages * kBTileBytes;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    // one CTA per SM (the kernel takes all 512 TMEM columns): ask for enough shared memory
+    // that a second CTA cannot be co-resident
+    const int want = 120 * 1024;
+    if ((err = cudaFuncSetAttribute(k_pf_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    want)) != cudaSuccess)
+      return err;
+    if ((err = cudaFuncSetAttribute(k_pf_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    want)) != cudaSuccess)
+      return err;
+    attr_set[dev] = true;
+  }
+  const size_t smem_launch = smem > 120 * 1024 ? smem : 120 * 1024;
+  PfGemmArgs g;
+  g.w = ex.w13; g.s = ex.s13; g.sh_w = ex.sh_w13; g.sh_s = ex.sh_s13; g.H = ex.H; g.I = ex.I;
+  g.T = T; g.hdr = I32(L.hdr); g.act_expert = I32(L.act_expert); g.group_act = I32(L.group_act);
+  g.group_p0 = I32(L.group_p0); g.group_n = I32(L.group_n); g.pair_tok = I32(L.pair_tok);
+  g.pair_w = F32(L.pair_w); g.act_g13 = nullptr; g.g13 = ex.g13; g.sh_g13 = ex.sh_g13;
+  g.b_src = reinterpret_cast<const __half*>(base + L.xf); g.xscale = F32(L.xscale);
+  g.h_out = reinterpret_cast<__half*>(base + L.h); g.part_out = nullptr; g.limit = limit;
+  g.oscale_mul = 1.0f / hscale; g.err = I32(L.err);
+  {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3(num_sms), dim3(kPfThreads), smem_launch, stream, at);
+    if ((err = cudaLaunchKernelEx(&cfg, k_pf_gemm<true>, g)) != cudaSuccess) return err;
+  }
+  PfGemmArgs g2 = g;
+  g2.w = ex.w2; g2.s = ex.s2; g2.sh_w = ex.sh_w2; g2.sh_s = ex.sh_s2;
+  g2.b_src = reinterpret_cast<const __half*>(base + L.h); g2.h_out = nullptr;
+  g2.part_out = reinterpret_cast<float*>(base + L.part);
+  {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3(num_sms), dim3(kPfThreads), smem_launch, stream, at);
+    if ((err = cudaLaunchKernelEx(&cfg, k_pf_gemm<false>, g2)) != cudaSuccess) return err;
+  }
+  PfReduceArgs ra;
+  ra.part = reinterpret_cast<const float*>(base + L.part); ra.pair_slot = I32(L.pair_slot);
+  ra.hdr = I32(L.hdr); ra.act_pair0 = I32(L.act_pair0); ra.T = T; ra.k = k; ra.H = ex.H;
+  ra.has_shared = shared ? 1 : 0; ra.out = out;
+  {
+    const long long n = (long long)T * ex.H / 8;
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, at);
+    if ((err = cudaLaunchKernelEx(&cfg, k_pf_reduce, ra)) != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace ftmoe

@@ -22,12 +22,13 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_UNSUPPORTED_SHAP
 
 EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_workspace_bytes",
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
-            "ft_moe_get_error"]
+            "ft_moe_get_error", "ft_moe_last_cuda_error"]
 
 
 class FtError(RuntimeError):
-    def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+    def __init__(self, status: int, what: str, detail: str = ""):
+        msg = f"{what}: {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.status = status
 
 
@@ -65,6 +66,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = layer
+    lib.ft_moe_last_cuda_error.restype = ctypes.c_char_p
     lib.ft_moe_get_error.restype = ctypes.c_int
     lib.ft_moe_get_error.argtypes = [vp, vp]
     return lib
@@ -89,7 +91,8 @@ def _stream(stream) -> int:
 
 def _check(st: int, what: str):
     if st != FT_OK:
-        raise FtError(st, what)
+        detail = _LIB.ft_moe_last_cuda_error().decode() if st == 5 else ""
+        raise FtError(st, what, detail)
 
 
 @dataclass
