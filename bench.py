@@ -38,8 +38,9 @@ NVFP4_BYTES_PER_ELEM = 0.5625       # 4-bit code + one E4M3 byte per 16 elements
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=480)
-    ap.add_argument("--warmup", type=int, default=48)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed layer calls (default: about a quarter second of GPU time)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--instances", type=int, default=None)
@@ -86,7 +87,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
                                           f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=subprocess.PIPE,
+                                          "-lms", "20"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -157,8 +158,8 @@ def run_ours(args, spec, rank, world, local):
     prefill = spec.prefill
     layers, exps, shs, wss, idxs, ws_ = [], [], [], [], [], []
     touched, pairs = [], []
-    for i in range(n_inst):
-        lay = make_device_layer(spec, instance=rank * n_inst + i, device=dev)
+    for inst in rank_instances(rank, n_inst):
+        lay = make_device_layer(spec, instance=inst, device=dev)
         ex = ftmoe.NvFP4Experts(lay.w13, lay.s13, lay.g13, lay.w2, lay.s2, lay.g2)
         sh = None
         if lay.shared is not None:
@@ -361,7 +362,8 @@ def run_reference(args, spec, rank, world, local):
     layers = [make_device_layer(spec, instance=i) for i in range(n_inst)]
     torch.cuda.synchronize()
     tokens = None if spec.T <= 32 else np.arange(16)
-    for s in range(args.warmup):
+    W = min(args.warmup, 2)          # the oracle is slow: a bounded warm-up
+    for s in range(W):
         oracle_call_seconds(spec, layers[s % n_inst], tokens)
     total, ntoks = 0.0, 0
     K = max(1, min(args.steps, 20))
@@ -376,7 +378,7 @@ def run_reference(args, spec, rank, world, local):
     sample = (f"{K} layer calls over instances 0-{n_inst - 1}"
               + ("" if tokens is None else f", {len(tokens)} of {spec.T} tokens per call, scaled"))
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
-            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": per_call * 1e3,
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": per_call * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32 (oracle)", "data": "synthetic",
             "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k,
@@ -395,19 +397,34 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """Max of a per-rank timing over all ranks (the slowest rank sets the job time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_instances(rank: int, n_inst: int):
+    """Layer instances a rank generates and times: ranks run independent replicas, each on
+    its own disjoint set of instances (weak scaling, no collective on the data path)."""
+    return [rank * n_inst + i for i in range(n_inst)]
+
+
+DEFAULT_STEPS = {1: 24000, 32: 240, 2048: 40}   # by batch size T
 
 
 def main():
     args = parse()
     from synth import BY_NAME
     spec = BY_NAME[args.workload]
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(spec.T, 480)
+    if args.warmup is None:
+        args.warmup = max(3, min(args.steps // 10, 480))
     rank, world, local = dist_env()
     if world > 1:
         import torch

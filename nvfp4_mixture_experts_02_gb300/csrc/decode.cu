@@ -24,10 +24,12 @@
 // bytes; an item cut by a CTA boundary is finished by the last CTA to arrive (a counter per
 // item), which adds the partial sums in CTA order. The output bits are reproducible.
 //
-// Pipelining. Every thread keeps kDepth chunks of its row's codes and of its share of the
-// activation tile in flight (registers); the activation tile goes to shared memory in the
-// K-major core-matrix layout; one thread issues the MMAs of a chunk and commits them to
-// the stage's mbarrier, so the dequantisation of chunk c+1 overlaps the MMAs of chunk c.
+// Pipelining. Every thread keeps kStages chunks of its row's codes and of its share of
+// the activation tile in flight (registers); the activation tile goes to shared memory in
+// the K-major core-matrix layout. Each thread arrives on the stage's "full" mbarrier when
+// its part of the chunk is in place; one thread waits for all of them, issues the chunk's
+// MMAs and commits them to the stage's "done" mbarrier. No CTA-wide barrier per chunk:
+// warps only wait before reusing a stage, so they can run kStages chunks apart.
 // Every device-side wait is bounded and reports FT_ERR_TIMEOUT instead of hanging.
 #include <cfloat>
 #include <cmath>
@@ -43,9 +45,9 @@ namespace {
 
 constexpr int kDT = 256;                 // threads: rows 0-127 of set 0 and of set 1
 constexpr int kDKc = 64;                 // reduction elements per chunk
-constexpr int kDepth = 6;                // chunks in flight per thread
+constexpr int kStages = 4;               // chunks in flight per thread = pipeline stages
 constexpr int kDNmax = 64;               // tokens per activation tile (T <= 64)
-constexpr uint32_t kDCols = 256;         // TMEM: D0 [0,64) D1 [64,128) A [128,256)
+constexpr uint32_t kDCols = 512;         // TMEM: D0 [0,64) D1 [64,128) A [128, 128+8*32)
 constexpr uint32_t kColD0 = 0, kColD1 = 64, kColA = 128;
 constexpr int kBTile = kDNmax * kDKc * 2;  // 8 KB per stage
 constexpr int kRowsPerItem = 256;
@@ -69,7 +71,8 @@ struct DecodeArgs {
   __half* xf;          // f16 activations: one private copy per CTA (small T) or one shared
   float* xscale_g;     // per-token activation scale and gate dot (shared copy)
   __half* h;           // SwiGLU outputs [pairs, I]
-  float* gpart;        // partial sums of items cut by a CTA boundary: [CTA][2][256][npad]
+  float* gpart;        // partial sums of items cut by a CTA boundary: [CTA][2][slot_floats]
+  int slot_floats;     // 256 rows x (T rounded up to 16) floats per slot
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -254,6 +257,58 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
   __syncthreads();
 }
 
+// The same plan for a single token, by warp 0 alone: the pairs are the valid slots in
+// slot order (k <= 32, one lane each), so no expert-wide counting is needed.
+__device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool has_shared = p.sh_g13 != nullptr;
+  if (tid < 32) {
+    const int k = p.k;
+    const int e = lane < k ? p.topk_idx[lane] : -1;
+    const float w = lane < k ? p.topk_w[lane] : 0.f;
+    bool ok = lane < k && e >= 0 && e < p.E;
+    for (int j = 0; j < k; ++j) {   // an id repeated in earlier slots is dropped
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      if (j < lane && ej == e) ok = false;
+    }
+    if (lane < k && !ok && blockIdx.x == 0) atomicOr(p.err, kErrBadExpert);
+    const unsigned vm = __ballot_sync(0xffffffffu, ok);
+    const int a = __popc(vm & ((1u << lane) - 1u));
+    const int n_routed = __popc(vm);
+    const float g2 = ok ? __ldg(p.g2 + e) : 0.f;
+    const float g13 = ok ? __ldg(p.g13 + e) : 0.f;
+    const float sg2 = has_shared ? __ldg(p.sh_g2) : 0.f;
+    float gmax = fmaxf(g2, sg2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    const float g2ref = gmax > 0.f ? gmax : 1.f;
+    if (ok) {
+      P.act_expert[a] = e;
+      P.act_pair0[a] = a;
+      P.act_g13[a] = g13;
+      P.pair_tok[a] = 0;
+      P.pair_wscale[a] = w * (g2 / g2ref) * p.hscale;
+    }
+    if (lane == 0) {
+      int n_act = n_routed;
+      if (has_shared) {
+        P.act_expert[n_act] = -1;
+        P.act_pair0[n_act] = n_act;
+        P.act_g13[n_act] = __ldg(p.sh_g13);
+        P.pair_tok[n_act] = 0;
+        ++n_act;
+      }
+      P.act_pair0[n_act] = n_act;
+      P.misc[0] = n_act;
+      P.misc[1] = n_act;
+      P.misc[2] = n_routed;
+      P.misc[3] = __float_as_int(g2ref);
+      P.misc[4] = __float_as_int(has_shared ? sg2 / g2ref : 0.f);
+    }
+  }
+  __syncthreads();
+}
+
 // f16 activations of token t scaled by a power of two (max |x| in [2^14, 2^15)), and the
 // shared-expert gate dot product, by the whole CTA; results through shared memory.
 __device__ void convert_token(const DecodeArgs& p, int t, __half* dst, float* s_scale,
@@ -322,23 +377,29 @@ __device__ __forceinline__ int split_owner(long long u, long long n, int P) {
 }
 
 // --------------------------------------------------------------- the split-K GEMM phase
-struct Stage {
-  uint64_t* mbar;       // [2]
-  uint32_t uses[2];     // commits issued per stage (mbarrier phase parity)
+// Stage bookkeeping. full[st] (kDT arrivals): every thread has written its A row chunk
+// into tensor memory and its activation pieces into shared memory; done[st] (one arrival,
+// from tcgen05.commit): the MMAs that read stage st have finished. Threads wait only
+// before reusing a stage, so warps run up to kStages chunks apart.
+struct Pipe {
+  uint64_t* full;
+  uint64_t* done;
+  uint32_t uses[kStages];
+  uint32_t n;            // chunks produced so far; stage = n % kStages
 };
 
-// One phase (W13 or W2) over this CTA's contiguous (item, chunk) range.
-template <bool kW13>
+// One phase (W13 when w13, else W2) over this CTA's contiguous (item, chunk) range. One
+// code path for both phases keeps the hot loop small.
 __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
-                          unsigned char* sB, Stage& S, int n_act, const __half* xsrc,
-                          volatile int* s_flag) {
+                          unsigned char* sB, Pipe& S, int n_act, const __half* xsrc,
+                          volatile int* s_flag, const bool w13, const bool x_on_chip) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int set = warp >> 2, m = (warp & 3) * 32 + (tid & 31);
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const int K = kW13 ? p.H : p.I;            // reduction length per expert
-  const int cpe = K / kDKc;                  // chunks per expert
-  const int n_items = kW13 ? n_act * (p.I / 128) : (p.H + kRowsPerItem - 1) / kRowsPerItem;
-  const int nch = kW13 ? cpe : n_act * cpe;  // chunks per item
+  const int K = w13 ? p.H : p.I;            // reduction length per expert
+  const int cpe = K / kDKc;                 // chunks per expert
+  const int n_items = w13 ? n_act * (p.I / 128) : (p.H + kRowsPerItem - 1) / kRowsPerItem;
+  const int nch = w13 ? cpe : n_act * cpe;  // chunks per item
   const long long U = (long long)n_items * nch;
   bool ok = true;
   if (U == 0) return ok;
@@ -347,6 +408,7 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
   if (cta >= G) return ok;
   const long long u0 = U * cta / G, u1 = U * (cta + 1) / G;
   const size_t rowb = (size_t)K / 2, srowb = (size_t)K / 16;
+  const size_t nrows13 = 2 * (size_t)p.I;
   const int T = p.T;
   int seg = 0;
 
@@ -356,42 +418,42 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
     const int c0 = (int)(u - ibase), c1 = (int)min((long long)nch, u1 - ibase);
     u = ibase + c1;
     // ---- item geometry
-    int a13 = 0, rb, nv, pair0 = 0;
-    const uint8_t* wrow = nullptr;
-    const uint8_t* srow = nullptr;
-    if (kW13) {
+    int a13 = 0, rb, nv, pair0 = 0, row;
+    bool row_ok = true;
+    if (w13) {
       a13 = item / (p.I / 128);
       rb = item - a13 * (p.I / 128);
-      const int e = P.act_expert[a13];
       pair0 = P.act_pair0[a13];
       nv = P.act_pair0[a13 + 1] - pair0;
-      const int row = (set == 0 ? 0 : p.I) + rb * 128 + m;
-      const size_t nrows = 2 * (size_t)p.I;
-      wrow = (e >= 0 ? p.w13 + (size_t)e * nrows * rowb : p.sh_w13) + (size_t)row * rowb;
-      srow = (e >= 0 ? p.s13 + (size_t)e * nrows * srowb : p.sh_s13) + (size_t)row * srowb;
+      row = (set == 0 ? 0 : p.I) + rb * 128 + m;
     } else {
       rb = item;
       nv = T;
+      row = rb * kRowsPerItem + set * 128 + m;   // W2 output row of this thread
+      row_ok = row < p.H;                         // the last W2 item may be short
+      if (!row_ok) row = 0;
     }
     const int npad = (nv + 15) & ~15;
-    const int row2 = rb * kRowsPerItem + set * 128 + m;   // W2 output row of this thread
-    const bool row_ok = kW13 || row2 < p.H;               // the last W2 item may be short
 
     // ---- register pipeline: codes, scales, activation pieces
-    uint4 qa[kDepth][2];
-    uint32_t qs[kDepth];
-    uint4 qb[kDepth][2];
+    uint4 qa[kStages][2];
+    uint32_t qs[kStages];
+    uint4 qb[kStages][2];
     auto issue = [&](int d, int c) {
-      const uint8_t* wr = wrow;
-      const uint8_t* sr = srow;
-      int cc = c, a = a13;
-      if (!kW13) {
+      int a = a13, cc = c;
+      if (!w13) {
         a = c / cpe;
         cc = c - a * cpe;
-        const int e = P.act_expert[a];
-        const int rr = row_ok ? row2 : 0;
-        wr = (e >= 0 ? p.w2 + (size_t)e * p.H * rowb : p.sh_w2) + (size_t)rr * rowb;
-        sr = (e >= 0 ? p.s2 + (size_t)e * p.H * srowb : p.sh_s2) + (size_t)rr * srowb;
+      }
+      const int e = P.act_expert[a];
+      const uint8_t* wr;
+      const uint8_t* sr;
+      if (w13) {
+        wr = (e >= 0 ? p.w13 + (size_t)e * nrows13 * rowb : p.sh_w13) + (size_t)row * rowb;
+        sr = (e >= 0 ? p.s13 + (size_t)e * nrows13 * srowb : p.sh_s13) + (size_t)row * srowb;
+      } else {
+        wr = (e >= 0 ? p.w2 + (size_t)e * p.H * rowb : p.sh_w2) + (size_t)row * rowb;
+        sr = (e >= 0 ? p.s2 + (size_t)e * p.H * srowb : p.sh_s2) + (size_t)row * srowb;
       }
       if (row_ok) {
         qa[d][0] = ldg_stream16(wr + (size_t)cc * 32);
@@ -408,7 +470,7 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
         uint4 v = make_uint4(0, 0, 0, 0);
         if (n < nv && i < npad * 8) {
           const __half* src = nullptr;
-          if (kW13) {
+          if (w13) {
             src = xsrc + (size_t)P.pair_tok[pair0 + n] * p.H + (size_t)cc * kDKc + 8 * j;
           } else {
             int pr = -1;
@@ -416,23 +478,27 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
               if (P.pair_tok[q] == n) pr = q;
             if (pr >= 0) src = p.h + (size_t)pr * p.I + (size_t)cc * kDKc + 8 * j;
           }
-          if (src) v = __ldcg(reinterpret_cast<const uint4*>(src));
+          if (src) {
+            if (w13 && x_on_chip) v = *reinterpret_cast<const uint4*>(src);   // shared memory
+            else v = __ldcg(reinterpret_cast<const uint4*>(src));             // written in-kernel
+          }
         }
         qb[d][r] = v;
       }
     };
 #pragma unroll
-    for (int d = 0; d < kDepth; ++d)
+    for (int d = 0; d < kStages; ++d)
       if (c0 + d < c1) issue(d, c0 + d);
 
-    for (int cb = c0; cb < c1 && ok; cb += kDepth) {
+    const uint32_t idesc = idesc_f16(128, npad);
+    for (int cb = c0; cb < c1 && ok; cb += kStages) {
 #pragma unroll
-      for (int d = 0; d < kDepth; ++d) {
+      for (int d = 0; d < kStages; ++d) {
         const int c = cb + d;
         if (c < c1 && ok) {
-          const int st = (int)((S.uses[0] + S.uses[1]) & 1u);
-          if (S.uses[st] > 0)
-            ok = mbar_wait(&S.mbar[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
+          const int st = (int)(S.n % kStages);
+          if (S.uses[st] > 0)   // the MMAs that last read this stage are done
+            ok = mbar_wait(&S.done[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
           tc_fence_after();
           uint32_t r[32];
           dequant64(qa[d][0], qa[d][1], qs[d], r);
@@ -446,14 +512,14 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
               *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = qb[d][rr];
             }
           }
-          if (c + kDepth < c1) issue(d, c + kDepth);
+          if (c + kStages < c1) issue(d, c + kStages);
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
-          __syncthreads();
-          if (tid == 0) {
+          mbar_arrive(&S.full[st]);
+          if (tid == 0) {   // all rows of this chunk are in place: issue its MMAs
+            ok = mbar_wait(&S.full[st], S.uses[st] & 1, p.err, kErrTimeout);
             tc_fence_after();
-            const uint32_t idesc = idesc_f16(128, npad);
             const uint32_t b0 = smem_addr(bt);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
@@ -462,16 +528,19 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
                 mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
                        tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
                        smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > c0 || ks > 0) ? 1u : 0u);
-            mma_commit(&S.mbar[st]);
+            mma_commit(&S.done[st]);
           }
+          if (warp == 0) ok = __shfl_sync(0xffffffffu, ok, 0);   // keep warps converged
           ++S.uses[st];
+          ++S.n;
         }
       }
     }
     // ---- drain: all MMAs of this segment done
-    for (int st = 0; st < 2 && ok; ++st)
-      if (S.uses[st] > 0) ok = mbar_wait(&S.mbar[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
+    for (int st = 0; st < kStages && ok; ++st)
+      if (S.uses[st] > 0) ok = mbar_wait(&S.done[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
     tc_fence_after();
+    ok = __syncthreads_and(ok) != 0;   // every thread agrees before the epilogue
     if (!ok) break;
 
     const bool complete = c0 == 0 && c1 == nch;
@@ -480,7 +549,7 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
     if (!complete) {
       // publish this CTA's partial [256 rows][npad], count, the last arriver finishes
       const int cslot = seg == 0 ? 0 : 1;
-      float* dst = p.gpart + ((size_t)cta * 2 + cslot) * kRowsPerItem * kDNmax +
+      float* dst = p.gpart + ((size_t)cta * 2 + cslot) * p.slot_floats +
                    (size_t)(set * 128 + m) * npad;
       for (int nb = 0; nb < npad; nb += 16) {
         uint32_t v[16];
@@ -490,7 +559,7 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
       }
       __threadfence();
       __syncthreads();
-      int* counters = kW13 ? p.cnt13 : p.cnt2;
+      int* counters = w13 ? p.cnt13 : p.cnt2;
       if (tid == 0) {
         const int old = atomicAdd(&counters[item], 1);
         const int cf = split_owner(ibase, U, G), cl = split_owner(ibase + nch - 1, U, G);
@@ -510,13 +579,13 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
         for (int j = 0; j < 16; ++j) acc[j] = 0.f;
         for (int cc = cf; cc <= cl; ++cc) {
           const int slot = ((U * cc / G) / nch == item) ? 0 : 1;
-          const float* src = p.gpart + ((size_t)cc * 2 + slot) * kRowsPerItem * kDNmax +
+          const float* src = p.gpart + ((size_t)cc * 2 + slot) * p.slot_floats +
                              (size_t)ridx * npad + nb;
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + j);
         }
       };
-      if (kW13) {
+      if (w13) {
         if (set == 0) {   // warps 0-3: gate row m and up row m of the item
           const float g13 = P.act_g13[a13];
           const int i_out = rb * 128 + m;
@@ -552,10 +621,10 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
         for (int nb = 0; nb < npad; nb += 16) {
           float dv[16];
           if (complete) {
-            uint32_t d[16];
-            tmem_ld16(tbase + lane_off + dcol + nb, d);
+            uint32_t dd[16];
+            tmem_ld16(tbase + lane_off + dcol + nb, dd);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) dv[j] = __uint_as_float(d[j]);
+            for (int j = 0; j < 16; ++j) dv[j] = __uint_as_float(dd[j]);
           } else {
             sum_rows(set * 128 + m, nb, dv);
           }
@@ -563,7 +632,7 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
           for (int j = 0; j < 16; ++j) {
             const int n = nb + j;
             if (n < nv && row_ok)
-              p.out[(size_t)n * p.H + row2] =
+              p.out[(size_t)n * p.H + row] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(dv[j] * oscale));
           }
         }
@@ -578,7 +647,8 @@ __device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
 
 __global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ DecodeArgs p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t mbar_full[kStages];
+  __shared__ __align__(8) uint64_t mbar_done[kStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_flag;
   __shared__ float s_scale, s_dot;
@@ -598,8 +668,10 @@ __global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ Decod
 
   if (warp == 0) tmem_alloc(&tmem_slot, kDCols);
   if (tid == 0) {
-    mbar_init(&mbar[0], 1);
-    mbar_init(&mbar[1], 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&mbar_full[st], kDT);
+      mbar_init(&mbar_done[st], 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -610,15 +682,16 @@ __global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ Decod
   griddep_launch_dependents();
   griddep_wait();   // routing results may come from the previous kernel
 
-  build_plan(p, P, scratch);
+  if (p.T == 1) build_plan_t1(p, P);
+  else build_plan(p, P, scratch);
   const int n_act = P.misc[0];
   const int n_routed = P.misc[2];
   const bool has_shared = p.sh_g13 != nullptr;
-  const bool private_x = p.T <= kDecodePrivateX;
-  __half* xsrc = private_x ? p.xf + (size_t)blockIdx.x * p.T * p.H : p.xf;
+  const bool private_x = decode_x_on_chip(p.T, p.H);
+  __half* xsrc = private_x ? reinterpret_cast<__half*>(smem_raw + L.xs) : p.xf;
 
-  // activations: every CTA converts all tokens into its own copy (small T), or the CTAs
-  // convert one token each into a shared copy (larger T), followed by a grid barrier
+  // activations: every CTA converts all tokens into its shared memory (small T), or the
+  // CTAs convert one token each into a shared global copy (larger T), then a grid barrier
   for (int t = private_x ? 0 : (int)blockIdx.x; t < p.T; t += private_x ? 1 : (int)gridDim.x) {
     convert_token(p, t, xsrc + (size_t)t * p.H, &s_scale, &s_dot);
     if (tid == 0) {
@@ -647,12 +720,14 @@ __global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ Decod
   __threadfence();
   __syncthreads();
 
-  Stage S;
-  S.mbar = mbar;
-  S.uses[0] = S.uses[1] = 0;
-  bool ok = run_phase<true>(p, P, tbase, sB, S, n_act, xsrc, &s_flag);
+  Pipe S;
+  S.full = mbar_full;
+  S.done = mbar_done;
+  for (int st = 0; st < kStages; ++st) S.uses[st] = 0;
+  S.n = 0;
+  bool ok = run_phase(p, P, tbase, sB, S, n_act, xsrc, &s_flag, true, private_x);
   grid_sync(p.bar, p.err);
-  if (ok) ok = run_phase<false>(p, P, tbase, sB, S, n_act, nullptr, &s_flag);
+  if (ok) ok = run_phase(p, P, tbase, sB, S, n_act, nullptr, &s_flag, false, private_x);
   (void)ok;
 
   tc_fence_before();
@@ -672,11 +747,10 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   bar = take(16);
   cnt13 = take(sizeof(int) * (size_t)max_act * (I / 128));
   cnt2 = take(sizeof(int) * (size_t)(H / kRowsPerItem + 1));   // ceil(H / 256) items
-  const size_t xcopies = T <= kDecodePrivateX ? (size_t)grid : 1;
-  xf = take(2 * (size_t)T * H * xcopies);
+  xf = take(decode_x_on_chip(T, H) ? 16 : 2 * (size_t)T * H);   // shared f16 copy otherwise
   xscale = take(sizeof(float) * 2 * (size_t)T);
   h = take(2 * (size_t)max_pairs * I);
-  gpart = take(sizeof(float) * (size_t)grid * 2 * kRowsPerItem * kDNmax);
+  gpart = take(sizeof(float) * (size_t)grid * 2 * kRowsPerItem * (size_t)((T + 15) & ~15));
   total = o;
 }
 
@@ -684,9 +758,8 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
   const int routed = T * k < E ? T * k : E;
   ma = routed + (shared ? 1 : 0);
   mp = T * k + (shared ? T : 0);
-  (void)H;
   (void)I;
-  size_t o = 2 * (size_t)kBTile;   // activation tiles first (1024-byte aligned base)
+  size_t o = (size_t)kStages * kBTile;   // activation tiles first (1024-byte aligned base)
   auto take = [&](size_t bytes) { size_t at = o; o = (o + bytes + 15) / 16 * 16; return at; };
   act_expert = take(4 * (size_t)ma);
   act_pair0 = take(4 * (size_t)(ma + 1));
@@ -696,6 +769,7 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
   xscale = take(4 * (size_t)T);
   misc = take(4 * 8);
   scratch = take((size_t)E * 8 + 4 + (size_t)T * k * 9 + 16);
+  xs = take(decode_x_on_chip(T, H) ? 2 * (size_t)T * H : 0);   // f16 activations on chip
   total = o;
 }
 
@@ -731,6 +805,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   a.xscale_g = reinterpret_cast<float*>(base + WL.xscale);
   a.h = reinterpret_cast<__half*>(base + WL.h);
   a.gpart = reinterpret_cast<float*>(base + WL.gpart);
+  a.slot_floats = kRowsPerItem * ((T + 15) & ~15);
 
   // one CTA per SM: the kernel is a cooperative persistent grid that owns the SM's
   // tensor memory; a large shared-memory request keeps a second CTA off the SM

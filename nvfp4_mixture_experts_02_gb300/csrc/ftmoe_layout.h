@@ -12,7 +12,7 @@ constexpr int kMaxDecodeT = 64;
 constexpr int kMaxGrid = 512;          // upper bound on the split-K grid (CTAs)
 constexpr int kChunk = 128;            // reduction elements per chunk (64 packed bytes/row)
 constexpr int kGemvWarps = 8;          // warps per CTA of the decode kernel
-constexpr int kDecodePrivateX = 8;             // T <= 8: every CTA keeps its own f16 x copy
+constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each CTA's smem up to this
 constexpr size_t kDecodeMinSmem = 120 * 1024;  // keeps the decode kernel at one CTA per SM
 
 // Error word bits (workspace offset 0).
@@ -20,6 +20,12 @@ constexpr int kErrBadExpert = 1;
 constexpr int kErrTimeout = 2;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Decode keeps the f16 activations in every CTA's shared memory when they are small;
+// otherwise the CTAs convert them into one shared global copy.
+__host__ __device__ inline bool decode_x_on_chip(int T, int H) {
+  return (size_t)T * (size_t)H * 2 <= kDecodeXOnChip;
+}
 
 // Byte offsets of every region inside a decode workspace (global memory, caller-owned),
 // 256-byte aligned. grid = the number of CTAs of the decode kernel.
@@ -34,7 +40,7 @@ struct DecodeLayout {
 struct DecodeSmem {
   int ma = 0, mp = 0;
   size_t act_expert = 0, act_pair0 = 0, act_g13 = 0, pair_tok = 0, pair_wscale = 0,
-         xscale = 0, misc = 0, scratch = 0, total = 0;
+         xscale = 0, misc = 0, scratch = 0, xs = 0, total = 0;
   __host__ __device__ DecodeSmem(int T, int k, int E, int H, int I, bool shared);
 };
 

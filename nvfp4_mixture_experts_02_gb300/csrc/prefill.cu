@@ -18,11 +18,13 @@
 // output. Each thread owns one weight row: it streams the row's packed E2M1 codes and E4M3
 // scales with 16-byte loads (4 chunks in flight), forms e2m1*e4m3 exactly in f16
 // (hardware conversions + one f16x2 multiply per pair) and writes it into tensor memory
-// (tcgen05.st) as the MMA's A operand. The activations of the group (B operand) are
-// gathered into shared memory in the canonical K-major core-matrix layout. One thread
-// issues tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group
-// size rounded up to 16, K=16 per instruction) and commits to an mbarrier per stage; two
-// stages let the dequantisation of chunk c+1 overlap the MMAs of chunk c.
+// (tcgen05.st) as the MMA's A operand. The activations of the group (B operand) travel
+// through the same register pipeline into shared memory, in the canonical K-major
+// core-matrix layout. Every thread arrives on the stage's "full" mbarrier when its part of
+// a chunk is in place; one thread waits for all of them and issues tcgen05.mma (kind::f16,
+// A from TMEM, B from shared memory, M=128, N = group size rounded up to 16, K=16 per
+// instruction), committing to the stage's "done" mbarrier. Four stages and no CTA-wide
+// barrier per chunk let the warps run ahead of the MMAs.
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -37,10 +39,9 @@ namespace {
 constexpr int kPfThreads = 256;          // 8 warps: rows 0-127 of set 0 / set 1
 constexpr int kPfN = 128;                // max tokens per group (MMA N)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
-constexpr int kPfStages = 2;
-constexpr int kPfDepth = 4;              // chunks of codes in flight per thread
+constexpr int kPfStages = 4;              // pipeline stages = chunks in flight per thread
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 x 32 columns
+constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 stages x 2 x 32 cols
 constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 16 KB per stage
 
 struct PfPlanArgs {
@@ -289,7 +290,8 @@ struct PfGemmArgs {
 template <bool kW13>
 __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant__ PfGemmArgs p) {
   extern __shared__ __align__(1024) unsigned char pf_smem[];
-  __shared__ __align__(8) uint64_t mbar[kPfStages];
+  __shared__ __align__(8) uint64_t mbar_full[kPfStages];
+  __shared__ __align__(8) uint64_t mbar_done[kPfStages];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int s_tok[kPfN];
   __shared__ float s_w[kPfN];
@@ -308,7 +310,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) mbar_init(&mbar[s], 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&mbar_full[s], kPfThreads);
+      mbar_init(&mbar_done[s], 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -323,10 +328,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   const int n_groups = p.hdr[1];
   const int K = kW13 ? p.H : p.I;
   const int nchunks = K / kPfKc;
-  const int blocks = kW13 ? p.I / 128 : p.H / 256;
+  const int blocks = kW13 ? p.I / 128 : (p.H + 255) / 256;   // the last W2 block may be short
   const int n_items = n_groups * blocks;
   const size_t rowb = (size_t)K / 2, srowb = (size_t)K / 16;
-  uint32_t uses[kPfStages] = {0, 0};   // completed-use count per stage (phase parity)
+  uint32_t uses[kPfStages] = {0, 0, 0, 0};   // uses issued per stage (mbarrier parity)
+  uint32_t nprod = 0;                         // chunks produced; stage = nprod % kPfStages
   bool ok = true;
 
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -339,6 +345,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     int row;
     if (kW13) row = (set == 0 ? 0 : p.I) + rb * 128 + m;
     else row = rb * 256 + set * 128 + m;
+    const bool row_ok = kW13 || row < p.H;   // rows past H read nothing and write nothing
+    if (!row_ok) row = 0;
     const size_t nrows = kW13 ? 2 * (size_t)p.I : (size_t)p.H;
     const uint8_t* wrow = (e >= 0 ? p.w + (size_t)e * nrows * rowb : p.sh_w) + (size_t)row * rowb;
     const uint8_t* srow = (e >= 0 ? p.s + (size_t)e * nrows * srowb : p.sh_s) + (size_t)row * srowb;
@@ -352,81 +360,84 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     }
     __syncthreads();
 
-    // register pipeline of packed codes + scales
-    uint4 q[kPfDepth][2];
-    uint32_t sc[kPfDepth];
-#pragma unroll
-    for (int d = 0; d < kPfDepth; ++d) {
-      if (d < nchunks) {
-        q[d][0] = ldg_stream16(wrow + (size_t)d * 32);
-        q[d][1] = ldg_stream16(wrow + (size_t)d * 32 + 16);
-        sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)d * 4));
+    // register pipeline: codes, scales and this thread's activation pieces, kPfStages deep
+    uint4 q[kPfStages][2];
+    uint32_t sc[kPfStages];
+    uint4 qb[kPfStages][4];
+    auto issue = [&](int d, int c) {
+      if (row_ok) {
+        q[d][0] = ldg_stream16(wrow + (size_t)c * 32);
+        q[d][1] = ldg_stream16(wrow + (size_t)c * 32 + 16);
+        sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)c * 4));
+      } else {
+        q[d][0] = q[d][1] = make_uint4(0, 0, 0, 0);
+        sc[d] = 0;
       }
-    }
-    for (int c0 = 0; c0 < nchunks && ok; c0 += kPfDepth) {
 #pragma unroll
-      for (int d = 0; d < kPfDepth; ++d) {
+      for (int r = 0; r < 4; ++r) {
+        const int i = tid + r * kPfThreads;
+        const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (i < npad * 8 && n < nv) {
+          const size_t src_row = kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n);
+          v = __ldcg(reinterpret_cast<const uint4*>(p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j));
+        }
+        qb[d][r] = v;
+      }
+    };
+#pragma unroll
+    for (int d = 0; d < kPfStages; ++d)
+      if (d < nchunks) issue(d, d);
+    const uint32_t idesc = idesc_f16(128, npad);
+    for (int c0 = 0; c0 < nchunks && ok; c0 += kPfStages) {
+#pragma unroll
+      for (int d = 0; d < kPfStages; ++d) {
         const int c = c0 + d;
         if (c < nchunks && ok) {
-          const int st = c & (kPfStages - 1);
-          // the MMAs that last read this stage's buffers must be done
-          if (uses[st] > 0 || c >= kPfStages) {
-            if (c >= kPfStages || uses[st] > 0) {
-              ok = mbar_wait(&mbar[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
-            }
-          }
+          const int st = (int)(nprod % kPfStages);
+          if (uses[st] > 0)   // the MMAs that last read this stage are done
+            ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
           tc_fence_after();
-          // A: dequantise this row's 64 elements into TMEM
           uint32_t r[32];
           dequant64(q[d][0], q[d][1], sc[d], r);
-          const int nx = c + kPfDepth;
-          if (nx < nchunks) {
-            q[d][0] = ldg_stream16(wrow + (size_t)nx * 32);
-            q[d][1] = ldg_stream16(wrow + (size_t)nx * 32 + 16);
-            sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)nx * 4));
-          }
           tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
-          // B: the group's activations for this chunk, K-major core-matrix layout
           unsigned char* bt = sB + st * kBTileBytes;
-          for (int i = tid; i < npad * 8; i += kPfThreads) {
-            const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (n < nv) {
-              const size_t src_row = kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n);
-              v = *reinterpret_cast<const uint4*>(p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j);
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int i = tid + rr * kPfThreads;
+            if (i < npad * 8) {
+              const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
+              *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = qb[d][rr];
             }
-            *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = v;
           }
+          if (c + kPfStages < nchunks) issue(d, c + kPfStages);
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
-          __syncthreads();
-          if (tid == 0) {
+          mbar_arrive(&mbar_full[st]);
+          if (tid == 0) {   // all rows of this chunk are in place: issue its MMAs
+            ok = mbar_wait(&mbar_full[st], uses[st] & 1, p.err, kErrTimeout);
             tc_fence_after();
-            const uint32_t idesc = idesc_f16(128, npad);
             const uint32_t b0 = smem_addr(bt);
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              const uint32_t dcol = s == 0 ? kColD0 : kColD1;
+            for (int s = 0; s < 2; ++s)
 #pragma unroll
-              for (int ks = 0; ks < kPfKc / 16; ++ks) {
-                mma_ts(tbase + dcol, tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
+              for (int ks = 0; ks < kPfKc / 16; ++ks)
+                mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
+                       tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
                        smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
-              }
-            }
-            mma_commit(&mbar[st]);
+            mma_commit(&mbar_done[st]);
           }
+          if (warp == 0) ok = __shfl_sync(0xffffffffu, ok, 0);   // keep warps converged
           ++uses[st];
+          ++nprod;
         }
       }
     }
     // all MMAs of this item done -> read the accumulators
-    if (ok) {
-      for (int st = 0; st < kPfStages; ++st) {
-        // the last use of each stage that was issued
-        if (uses[st] > 0) ok = ok && mbar_wait(&mbar[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
-      }
-    }
+    for (int st = 0; st < kPfStages && ok; ++st)
+      if (uses[st] > 0) ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
+    ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
     if (ok) {
       if (kW13) {
@@ -458,7 +469,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int n = nb + j;
-            if (n < nv) {
+            if (n < nv && row_ok) {
               p.part_out[(size_t)(p0 + n) * p.H + r_out] = __uint_as_float(dv[j]) * oscale;
             }
           }
