@@ -1,56 +1,61 @@
-// Decode path of the NVFP4 MoE layer (1 <= T <= 64) as ONE persistent kernel on the
-// 5th-generation tensor cores:
+// Decode path of the NVFP4 MoE layer (1 <= T <= 64) as ONE persistent cooperative kernel:
 //
-//   plan (every CTA, shared memory) -> W13 + clamped SwiGLU -> grid barrier -> W2 +
-//   router-weighted top-k sum
+//   plan (every CTA, shared memory) -> f16 activations -> W13 + clamped SwiGLU
+//   -> grid barrier -> W2 + router-weighted top-k sum [-> grid barrier -> per-token sum]
 //
-// Arithmetic. An NVFP4 weight is e2m1(code) * e4m3(block scale) * tensor scale. The first
-// product has at most 6 significant bits and lies in [2^-10, 2688], so it is an exact f16.
-// Each thread owns one weight row: it streams the row's packed codes and scales with
-// 16-byte loads, forms e2m1*e4m3 with the hardware E2M1->f16x2 / E4M3->f16x2 conversions
-// and one f16x2 multiply per pair, and writes it into tensor memory as the A operand of
-// tcgen05.mma (kind::f16, M = 128 rows, N = the expert's tokens rounded up to 16, fp32
-// accumulators in tensor memory). The tensor scale multiplies the fp32 sums. Activations
-// enter as f16 scaled per token by a power of two (exact for bf16 data); the SwiGLU output
-// h is stored as f16 pre-multiplied by its router weight, the ratio of its W2 tensor scale
-// to a per-call reference, and 2^S with 2^S * L^2 < 65504 (|h| < L^2 for the clamped SwiGLU).
+// At decode sizes every (token, expert) pair sees a handful of tokens, so the work is a
+// batch of matrix-vector products bound by the weight stream; it runs on the CUDA cores as
+// a coalesced GEMV, with no block-wide barrier anywhere in the hot loop.
 //
-// Work split. A W13 item is 128 gate rows and the 128 matching up rows of one active
-// expert (two accumulators, so the SwiGLU pair of every output sits in one TMEM lane); a
-// W2 item is 256 output rows whose reduction runs over (active expert, i), with the router
-// weights already folded into h, so one long sum gives the weighted top-k sum plus the
-// shared expert with no separate reduction launch. (item, 64-element chunk) units are cut
-// into equal contiguous ranges, one per CTA, so every SM streams the same number of weight
-// bytes; an item cut by a CTA boundary is finished by the last CTA to arrive (a counter per
-// item), which adds the partial sums in CTA order. The output bits are reproducible.
+// Arithmetic. An NVFP4 weight is e2m1(code) * e4m3(block scale) * tensor scale. A warp
+// step covers 1024 elements of two weight rows: each lane loads 16 bytes (32 codes) of
+// each row plus their two block scales, converts the codes with the hardware E2M1->f16x2
+// instruction (exact) and accumulates code * activation over one 16-element block in f16
+// (f16x2 FMA; the activations are scaled so that no block sum can leave the f16 range).
+// The block sum is scaled by its E4M3 scale into an fp32 accumulator; the tensor scale
+// multiplies the fp32 total. Activations are f16 rows scaled per token by a power of two
+// (max |x| in [256, 512), exact for bf16 data); the SwiGLU output h is stored as f16
+// pre-multiplied by its router weight, the ratio of its W2 tensor scale to a per-call
+// reference, and 2^S with 2^S * L^2 <= 512 (|h| < L^2 for the clamped SwiGLU).
 //
-// Pipelining. Every thread keeps kStages chunks of its row's codes and of its share of
-// the activation tile in flight (registers); the activation tile goes to shared memory in
-// the K-major core-matrix layout. Each thread arrives on the stage's "full" mbarrier when
-// its part of the chunk is in place; one thread waits for all of them, issues the chunk's
-// MMAs and commits them to the stage's "done" mbarrier. No CTA-wide barrier per chunk:
-// warps only wait before reusing a stage, so they can run kStages chunks apart.
+// Work split. W13 unit = gate row j and up row j of one segment (a run of at most NT of
+// one expert's pairs), so the SwiGLU pair of every output lands in one warp. W2 unit = a
+// pair of output rows: for one token (NT == 1) its reduction runs over (active expert, i)
+// with the router weights already folded into h, so one sum yields the weighted top-k sum
+// plus the shared expert; for several tokens it runs over one segment's pairs and the
+// per-pair results are summed per token after a last grid barrier. The (unit, step) list
+// of a phase is cut into equal contiguous ranges, one per warp of the grid, so every warp
+// streams the same number of weight bytes; a unit cut by a range boundary is finished by
+// the last warp to arrive (a counter per split unit), which adds the partial sums in warp
+// order. The output bits are reproducible for a given device.
+//
 // Every device-side wait is bounded and reports FT_ERR_TIMEOUT instead of hanging.
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ftmoe_device.cuh"
 #include "ftmoe_internal.h"
-#include "ftmoe_tc.cuh"
 
 namespace ftmoe {
 
 namespace {
 
-constexpr int kDT = 256;                 // threads: rows 0-127 of set 0 and of set 1
-constexpr int kDKc = 64;                 // reduction elements per chunk
-constexpr int kStages = 4;               // chunks in flight per thread = pipeline stages
-constexpr int kDNmax = 64;               // tokens per activation tile (T <= 64)
-constexpr uint32_t kDCols = 512;         // TMEM: D0 [0,64) D1 [64,128) A [128, 128+8*32)
-constexpr uint32_t kColD0 = 0, kColD1 = 64, kColA = 128;
-constexpr int kBTile = kDNmax * kDKc * 2;  // 8 KB per stage
-constexpr int kRowsPerItem = 256;
+template <int NT>
+struct Warps {   // warps per CTA
+  static constexpr int value = NT == 1 ? 16 : 8;
+};
+constexpr int kStepElems = 1024;   // reduction elements of one warp step (32 per lane)
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+enum Mode { kW13 = 0, kW2Rows = 1, kW2Seg = 2 };
+
+// Relative cost of one warp step over a segment of nv tokens: kCostBase + kCostTok * nv
+// (the weight conversion is shared, the dot products are per token). Warp ranges are
+// cut to equal cost, not to equal step counts.
+constexpr int kCostBase = 3, kCostTok = 2;
+__device__ __forceinline__ int step_cost(int nv) { return kCostBase + kCostTok * nv; }
 
 struct DecodeArgs {
   const uint16_t* x;
@@ -65,45 +70,62 @@ struct DecodeArgs {
   float limit, hscale, inv_hscale;
   uint16_t* out;
   int* err;
-  unsigned* bar;       // grid barrier: [0] arrivals, [1] generation
-  int* cnt13;          // per W13 item: CTAs arrived
-  int* cnt2;           // per W2 item
-  __half* xf;          // f16 activations: one private copy per CTA (small T) or one shared
-  float* xscale_g;     // per-token activation scale and gate dot (shared copy)
-  __half* h;           // SwiGLU outputs [pairs, I]
-  float* gpart;        // partial sums of items cut by a CTA boundary: [CTA][2][slot_floats]
-  int slot_floats;     // 256 rows x (T rounded up to 16) floats per slot
+  unsigned long long* bar;   // grid barrier: monotonic arrival counter
+  int* cnt;         // arrivals per split unit, indexed by the unit's first warp
+  __half* xf;       // f16 activations, one shared copy (when they do not fit on chip)
+  float* xscale_g;  // per-token activation scale and shared-gate dot (shared copy)
+  __half* h;        // SwiGLU outputs [pairs][I]
+  float* gpart;     // partial sums of split units: [warp][2 slots][2 * NT]
+  float* part;      // several tokens: W2 result per (pair, output row) [pairs][H]
+  int smem_bytes;   // dynamic shared memory granted to each CTA
 };
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Byte offset of activation element e in a padded row (32 elements per 80 bytes).
+__device__ __forceinline__ int act_byte(int e) { return (e >> 5) * kActGroupBytes + (e & 31) * 2; }
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Barrier over the whole (co-resident, cooperative) grid; bounded wait.
-__device__ void grid_sync(unsigned* bar, int* err) {
+// Grid barrier on a monotonic 64-bit arrival counter: barrier b of a launch completes when
+// the counter reaches base + (b + 1) * gridDim.x, base = its value when the launch began
+// (every launch adds gridDim.x per barrier, so base is a multiple of it). One release
+// add per CTA, no release step, no reset; the wait is bounded.
+__device__ void grid_sync(unsigned long long* bar, unsigned long long target, int* err) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
-      unsigned it = 0;
-      while (ld_acquire(bar + 1) == gen) {
-        if (++it > kSpinLimit) {
-          atomicOr(err, kErrTimeout);
-          break;
-        }
-        __nanosleep(32);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+    unsigned it = 0;
+    while ((long long)(ld_acquire64(bar) - target) < 0) {
+      if (++it > kSpinLimit) {
+        atomicOr(err, kErrTimeout);
+        break;
       }
+      __nanosleep(20);
     }
-    __threadfence();
   }
   __syncthreads();
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// lo + hi of an f16x2 word, as fp32 (the sum is formed in f16: both halves of a block sum
+// are below 2^15 in magnitude, so it cannot overflow).
+__device__ __forceinline__ float hsum2(uint32_t v) {
+  const __half2 h2 = *reinterpret_cast<const __half2*>(&v);
+  return __half2float(__hadd(__low2half(h2), __high2half(h2)));
 }
 
 // ---------------------------------------------------------------------------- plan
@@ -115,6 +137,11 @@ struct Plan {
   float* pair_wscale; // router weight * (W2 scale / reference) * 2^S
   float* xscale;      // per-token activation scale
   int* misc;          // [0] n_act [1] n_pairs [2] n_routed [3] ref. W2 scale [4] shared ratio
+                      // [5] n_seg
+  int* seg_act;       // active expert of each segment
+  int* seg_pair0;     // first pair of each segment; [n_seg] = n_pairs
+  int* seg_cp;        // cost prefix: sum over earlier segments of the cost of one step
+  int* tok_pairs;     // [T][k + 1]: pairs of each token in slot order, shared last, -1 = none
 };
 
 __device__ int block_exclusive_scan(int v, int* tmp, int& total) {
@@ -147,6 +174,7 @@ __device__ int block_exclusive_scan(int v, int* tmp, int& total) {
 
 // Every CTA builds the same plan from topk_idx / topk_w in its shared memory. The routing
 // arrays are read once, in parallel, into shared memory first.
+template <int NT>
 __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int T = p.T, k = p.k, E = p.E, TK = T * k;
@@ -157,7 +185,7 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
   float* sw = reinterpret_cast<float*>(scratch + 2 * E + 1 + TK);  // [T*k]
   unsigned char* okq = reinterpret_cast<unsigned char*>(scratch + 2 * E + 1 + 2 * TK);
   __shared__ int scan_tmp[33];
-  __shared__ float red[32];
+  __shared__ float red[32], wred[32];
 
   for (int q = tid; q < TK; q += nthr) {
     sidx[q] = p.topk_idx[q];
@@ -165,14 +193,19 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
   }
   for (int e = tid; e < E; e += nthr) cnt[e] = 0;
   __syncthreads();
+  float wmax = 1.f;   // router weights above 1 shrink every pair's h scale alike
   for (int q = tid; q < TK; q += nthr) {
     const int t = q / k, j = q - t * k;
     const int e = sidx[q];
     bool ok = e >= 0 && e < E;
     for (int jj = 0; jj < j && ok; ++jj) ok = sidx[t * k + jj] != e;
     okq[q] = ok ? 1 : 0;
-    if (ok) atomicAdd(&cnt[e], 1);
-    else if (blockIdx.x == 0) atomicOr(p.err, kErrBadExpert);
+    if (ok) {
+      atomicAdd(&cnt[e], 1);
+      wmax = fmaxf(wmax, fabsf(sw[q]));
+    } else if (blockIdx.x == 0) {
+      atomicOr(p.err, kErrBadExpert);
+    }
   }
   __syncthreads();
 
@@ -218,16 +251,28 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
     gmax = fmaxf(gmax, g2);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-  if ((tid & 31) == 0) red[tid >> 5] = gmax;
+  for (int o = 16; o > 0; o >>= 1) {
+    gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+  }
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = gmax;
+    wred[tid >> 5] = wmax;
+  }
   __syncthreads();
   if (tid < 32) {
     float v = tid < (nthr >> 5) ? red[tid] : 0.f;
+    float wv = tid < (nthr >> 5) ? wred[tid] : 1.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (tid == 0) red[0] = v > 0.f ? v : 1.f;
+    for (int o = 16; o > 0; o >>= 1) {
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      wv = fmaxf(wv, __shfl_xor_sync(0xffffffffu, wv, o));
+    }
+    if (tid == 0) red[0] = (v > 0.f ? v : 1.f) * wv;
   }
   __syncthreads();
+  // reference = largest W2 tensor scale * max(1, largest router weight): every pair's
+  // weight * W2 scale / reference is at most 1, which bounds the stored h
   const float g2ref = red[0];
   // keep each active expert's W2 scale ratio before pair_wscale is overwritten
   float* g2ratio = reinterpret_cast<float*>(cnt);   // reuse: the counts are no longer needed
@@ -235,8 +280,11 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
   __syncthreads();
 
   for (int q = tid; q < TK; q += nthr) {
-    if (!okq[q]) continue;
-    const int t = q / k;
+    const int t = q / k, j = q - t * k;
+    if (!okq[q]) {
+      P.tok_pairs[t * (k + 1) + j] = -1;
+      continue;
+    }
     const int e = sidx[q];
     int rank = 0;
     for (int q2 = 0; q2 < t * k; ++q2) rank += (okq[q2] && sidx[q2] == e);
@@ -244,21 +292,50 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
     const int pos = P.act_pair0[ai] + rank;
     P.pair_tok[pos] = t;
     P.pair_wscale[pos] = sw[q] * g2ratio[ai] * p.hscale;
+    P.tok_pairs[t * (k + 1) + j] = pos;
   }
-  if (has_shared)
-    for (int t = tid; t < T; t += nthr) P.pair_tok[n_pairs_routed + t] = t;
+  for (int t = tid; t < T; t += nthr) {
+    if (has_shared) P.pair_tok[n_pairs_routed + t] = t;
+    P.tok_pairs[t * (k + 1) + k] = has_shared ? n_pairs_routed + t : -1;
+  }
+
+  // segments: each active expert's pairs cut into runs of at most NT
+  const int pa = (n_act + nthr - 1) / nthr;
+  const int a_begin = min(n_act, tid * pa), a_end = min(n_act, a_begin + pa);
+  int ng = 0;
+  for (int i = a_begin; i < a_end; ++i) ng += (P.act_pair0[i + 1] - P.act_pair0[i] + NT - 1) / NT;
+  int n_seg;
+  int so = block_exclusive_scan(ng, scan_tmp, n_seg);
+  int cost = 0;   // this thread's segments, in order
+  for (int i = a_begin; i < a_end; ++i)
+    for (int q = P.act_pair0[i]; q < P.act_pair0[i + 1]; q += NT)
+      cost += step_cost(min(NT, P.act_pair0[i + 1] - q));
+  int c_total;
+  int co = block_exclusive_scan(cost, scan_tmp, c_total);
+  for (int i = a_begin; i < a_end; ++i) {
+    for (int q = P.act_pair0[i]; q < P.act_pair0[i + 1]; q += NT) {
+      P.seg_act[so] = i;
+      P.seg_pair0[so] = q;
+      P.seg_cp[so] = co;
+      co += step_cost(min(NT, P.act_pair0[i + 1] - q));
+      ++so;
+    }
+  }
   if (tid == 0) {
+    P.seg_pair0[n_seg] = n_pairs;
+    P.seg_cp[n_seg] = c_total;
     P.misc[0] = n_act;
     P.misc[1] = n_pairs;
     P.misc[2] = n_routed;
     P.misc[3] = __float_as_int(g2ref);
     P.misc[4] = __float_as_int(has_shared ? g2ratio[n_routed] : 0.f);
+    P.misc[5] = n_seg;
   }
   __syncthreads();
 }
 
 // The same plan for a single token, by warp 0 alone: the pairs are the valid slots in
-// slot order (k <= 32, one lane each), so no expert-wide counting is needed.
+// slot order (k <= 32, one lane each), one segment per active expert.
 __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
   const int tid = threadIdx.x, lane = tid & 31;
   const bool has_shared = p.sh_g13 != nullptr;
@@ -278,16 +355,21 @@ __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
     const float g2 = ok ? __ldg(p.g2 + e) : 0.f;
     const float g13 = ok ? __ldg(p.g13 + e) : 0.f;
     const float sg2 = has_shared ? __ldg(p.sh_g2) : 0.f;
-    float gmax = fmaxf(g2, sg2);
+    float gmax = fmaxf(g2, sg2), wmax = ok ? fmaxf(1.f, fabsf(w)) : 1.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-    const float g2ref = gmax > 0.f ? gmax : 1.f;
+    for (int o = 16; o > 0; o >>= 1) {
+      gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+    }
+    const float g2ref = (gmax > 0.f ? gmax : 1.f) * wmax;
     if (ok) {
       P.act_expert[a] = e;
       P.act_pair0[a] = a;
       P.act_g13[a] = g13;
       P.pair_tok[a] = 0;
       P.pair_wscale[a] = w * (g2 / g2ref) * p.hscale;
+      P.seg_act[a] = a;
+      P.seg_pair0[a] = a;
     }
     if (lane == 0) {
       int n_act = n_routed;
@@ -296,22 +378,26 @@ __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
         P.act_pair0[n_act] = n_act;
         P.act_g13[n_act] = __ldg(p.sh_g13);
         P.pair_tok[n_act] = 0;
+        P.seg_act[n_act] = n_act;
+        P.seg_pair0[n_act] = n_act;
         ++n_act;
       }
       P.act_pair0[n_act] = n_act;
+      P.seg_pair0[n_act] = n_act;
       P.misc[0] = n_act;
       P.misc[1] = n_act;
       P.misc[2] = n_routed;
       P.misc[3] = __float_as_int(g2ref);
       P.misc[4] = __float_as_int(has_shared ? sg2 / g2ref : 0.f);
+      P.misc[5] = n_act;
     }
   }
   __syncthreads();
 }
 
-// f16 activations of token t scaled by a power of two (max |x| in [2^14, 2^15)), and the
-// shared-expert gate dot product, by the whole CTA; results through shared memory.
-__device__ void convert_token(const DecodeArgs& p, int t, __half* dst, float* s_scale,
+// f16 activations of token t scaled by a power of two (max |x| in [256, 512)), stored as a
+// padded row, and the shared-expert gate dot product, by the whole CTA.
+__device__ void convert_token(const DecodeArgs& p, int t, char* dst, float* s_scale,
                               float* s_dot) {
   __shared__ float red_a[32], red_d[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -348,8 +434,8 @@ __device__ void convert_token(const DecodeArgs& p, int t, __half* dst, float* s_
     }
     int ex = 0;
     if (a > 0.f) {
-      frexpf(a, &ex);
-      ex -= 15;
+      frexpf(a, &ex);   // a = m * 2^ex, m in [0.5, 1)
+      ex -= 9;          // a / 2^ex in [256, 512)
     }
     *s_scale = ldexpf(1.f, ex);
     *s_dot = d;
@@ -366,296 +452,625 @@ __device__ void convert_token(const DecodeArgs& p, int t, __half* dst, float* s_
                                            __uint_as_float(w[j] & 0xFFFF0000u) * down);
       o[j] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    *reinterpret_cast<uint4*>(dst + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + act_byte(c)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   __syncthreads();
 }
 
-// range(i) = [n*i/P, n*(i+1)/P); owner(u) = the i whose range holds u (0 <= u < n).
-__device__ __forceinline__ int split_owner(long long u, long long n, int P) {
-  return (int)(((u + 1) * P - 1) / n);
-}
-
-// --------------------------------------------------------------- the split-K GEMM phase
-// Stage bookkeeping. full[st] (kDT arrivals): every thread has written its A row chunk
-// into tensor memory and its activation pieces into shared memory; done[st] (one arrival,
-// from tcgen05.commit): the MMAs that read stage st have finished. Threads wait only
-// before reusing a stage, so warps run up to kStages chunks apart.
-struct Pipe {
-  uint64_t* full;
-  uint64_t* done;
-  uint32_t uses[kStages];
-  uint32_t n;            // chunks produced so far; stage = n % kStages
+// Single token: this thread's 16-byte chunks of x and of the shared-expert gate, loaded
+// into registers before the weight stream starts so that they are not queued behind it.
+constexpr int kXChunks = 4;   // H <= 16384 elements over 512 threads
+struct XRegs {
+  uint4 x[kXChunks], g[kXChunks];
 };
 
-// One phase (W13 when w13, else W2) over this CTA's contiguous (item, chunk) range. One
-// code path for both phases keeps the hot loop small.
-__device__ bool run_phase(const DecodeArgs& p, const Plan& P, uint32_t tbase,
-                          unsigned char* sB, Pipe& S, int n_act, const __half* xsrc,
-                          volatile int* s_flag, const bool w13, const bool x_on_chip) {
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int set = warp >> 2, m = (warp & 3) * 32 + (tid & 31);
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const int K = w13 ? p.H : p.I;            // reduction length per expert
-  const int cpe = K / kDKc;                 // chunks per expert
-  const int n_items = w13 ? n_act * (p.I / 128) : (p.H + kRowsPerItem - 1) / kRowsPerItem;
-  const int nch = w13 ? cpe : n_act * cpe;  // chunks per item
-  const long long U = (long long)n_items * nch;
-  bool ok = true;
-  if (U == 0) return ok;
-  const int G = (int)min((long long)gridDim.x, U);
-  const int cta = blockIdx.x;
-  if (cta >= G) return ok;
-  const long long u0 = U * cta / G, u1 = U * (cta + 1) / G;
-  const size_t rowb = (size_t)K / 2, srowb = (size_t)K / 16;
-  const size_t nrows13 = 2 * (size_t)p.I;
-  const int T = p.T;
-  int seg = 0;
-
-  for (long long u = u0; u < u1 && ok;) {
-    const int item = (int)(u / nch);
-    const long long ibase = (long long)item * nch;
-    const int c0 = (int)(u - ibase), c1 = (int)min((long long)nch, u1 - ibase);
-    u = ibase + c1;
-    // ---- item geometry
-    int a13 = 0, rb, nv, pair0 = 0, row;
-    bool row_ok = true;
-    if (w13) {
-      a13 = item / (p.I / 128);
-      rb = item - a13 * (p.I / 128);
-      pair0 = P.act_pair0[a13];
-      nv = P.act_pair0[a13 + 1] - pair0;
-      row = (set == 0 ? 0 : p.I) + rb * 128 + m;
-    } else {
-      rb = item;
-      nv = T;
-      row = rb * kRowsPerItem + set * 128 + m;   // W2 output row of this thread
-      row_ok = row < p.H;                         // the last W2 item may be short
-      if (!row_ok) row = 0;
+__device__ void x_t1_load(const DecodeArgs& p, XRegs& r) {
+#pragma unroll
+  for (int c = 0; c < kXChunks; ++c) {
+    const int e = (threadIdx.x + c * blockDim.x) * 8;
+    r.x[c] = r.g[c] = make_uint4(0, 0, 0, 0);
+    if (e < p.H) {
+      r.x[c] = *reinterpret_cast<const uint4*>(p.x + e);
+      if (p.sh_gate) r.g[c] = *reinterpret_cast<const uint4*>(p.sh_gate + e);
     }
-    const int npad = (nv + 15) & ~15;
-
-    // ---- register pipeline: codes, scales, activation pieces
-    uint4 qa[kStages][2];
-    uint32_t qs[kStages];
-    uint4 qb[kStages][2];
-    auto issue = [&](int d, int c) {
-      int a = a13, cc = c;
-      if (!w13) {
-        a = c / cpe;
-        cc = c - a * cpe;
-      }
-      const int e = P.act_expert[a];
-      const uint8_t* wr;
-      const uint8_t* sr;
-      if (w13) {
-        wr = (e >= 0 ? p.w13 + (size_t)e * nrows13 * rowb : p.sh_w13) + (size_t)row * rowb;
-        sr = (e >= 0 ? p.s13 + (size_t)e * nrows13 * srowb : p.sh_s13) + (size_t)row * srowb;
-      } else {
-        wr = (e >= 0 ? p.w2 + (size_t)e * p.H * rowb : p.sh_w2) + (size_t)row * rowb;
-        sr = (e >= 0 ? p.s2 + (size_t)e * p.H * srowb : p.sh_s2) + (size_t)row * srowb;
-      }
-      if (row_ok) {
-        qa[d][0] = ldg_stream16(wr + (size_t)cc * 32);
-        qa[d][1] = ldg_stream16(wr + (size_t)cc * 32 + 16);
-        qs[d] = __ldg(reinterpret_cast<const uint32_t*>(sr + (size_t)cc * 4));
-      } else {
-        qa[d][0] = qa[d][1] = make_uint4(0, 0, 0, 0);
-        qs[d] = 0;
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int i = tid + r * kDT;
-        const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < nv && i < npad * 8) {
-          const __half* src = nullptr;
-          if (w13) {
-            src = xsrc + (size_t)P.pair_tok[pair0 + n] * p.H + (size_t)cc * kDKc + 8 * j;
-          } else {
-            int pr = -1;
-            for (int q = P.act_pair0[a]; q < P.act_pair0[a + 1]; ++q)
-              if (P.pair_tok[q] == n) pr = q;
-            if (pr >= 0) src = p.h + (size_t)pr * p.I + (size_t)cc * kDKc + 8 * j;
-          }
-          if (src) {
-            if (w13 && x_on_chip) v = *reinterpret_cast<const uint4*>(src);   // shared memory
-            else v = __ldcg(reinterpret_cast<const uint4*>(src));             // written in-kernel
-          }
-        }
-        qb[d][r] = v;
-      }
-    };
-#pragma unroll
-    for (int d = 0; d < kStages; ++d)
-      if (c0 + d < c1) issue(d, c0 + d);
-
-    const uint32_t idesc = idesc_f16(128, npad);
-    for (int cb = c0; cb < c1 && ok; cb += kStages) {
-#pragma unroll
-      for (int d = 0; d < kStages; ++d) {
-        const int c = cb + d;
-        if (c < c1 && ok) {
-          const int st = (int)(S.n % kStages);
-          if (S.uses[st] > 0)   // the MMAs that last read this stage are done
-            ok = mbar_wait(&S.done[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
-          tc_fence_after();
-          uint32_t r[32];
-          dequant64(qa[d][0], qa[d][1], qs[d], r);
-          tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
-          unsigned char* bt = sB + st * kBTile;
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int i = tid + rr * kDT;
-            if (i < npad * 8) {
-              const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
-              *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = qb[d][rr];
-            }
-          }
-          if (c + kStages < c1) issue(d, c + kStages);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          tc_fence_before();
-          mbar_arrive(&S.full[st]);
-          if (tid == 0) {   // all rows of this chunk are in place: issue its MMAs
-            ok = mbar_wait(&S.full[st], S.uses[st] & 1, p.err, kErrTimeout);
-            tc_fence_after();
-            const uint32_t b0 = smem_addr(bt);
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-#pragma unroll
-              for (int ks = 0; ks < kDKc / 16; ++ks)
-                mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
-                       tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
-                       smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > c0 || ks > 0) ? 1u : 0u);
-            mma_commit(&S.done[st]);
-          }
-          if (warp == 0) ok = __shfl_sync(0xffffffffu, ok, 0);   // keep warps converged
-          ++S.uses[st];
-          ++S.n;
-        }
-      }
-    }
-    // ---- drain: all MMAs of this segment done
-    for (int st = 0; st < kStages && ok; ++st)
-      if (S.uses[st] > 0) ok = mbar_wait(&S.done[st], (S.uses[st] - 1) & 1, p.err, kErrTimeout);
-    tc_fence_after();
-    ok = __syncthreads_and(ok) != 0;   // every thread agrees before the epilogue
-    if (!ok) break;
-
-    const bool complete = c0 == 0 && c1 == nch;
-    const uint32_t dcol = set == 0 ? kColD0 : kColD1;
-    bool finish = complete;
-    if (!complete) {
-      // publish this CTA's partial [256 rows][npad], count, the last arriver finishes
-      const int cslot = seg == 0 ? 0 : 1;
-      float* dst = p.gpart + ((size_t)cta * 2 + cslot) * p.slot_floats +
-                   (size_t)(set * 128 + m) * npad;
-      for (int nb = 0; nb < npad; nb += 16) {
-        uint32_t v[16];
-        tmem_ld16(tbase + lane_off + dcol + nb, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) dst[nb + j] = __uint_as_float(v[j]);
-      }
-      __threadfence();
-      __syncthreads();
-      int* counters = w13 ? p.cnt13 : p.cnt2;
-      if (tid == 0) {
-        const int old = atomicAdd(&counters[item], 1);
-        const int cf = split_owner(ibase, U, G), cl = split_owner(ibase + nch - 1, U, G);
-        *s_flag = old == cl - cf;
-        if (old == cl - cf) counters[item] = 0;   // ready for the next call
-      }
-      __syncthreads();
-      finish = *s_flag != 0;
-      if (finish) __threadfence();
-    }
-    if (finish) {
-      // the item's full sums: from TMEM (complete) or the CTAs' partials in CTA order
-      const int cf = complete ? cta : split_owner(ibase, U, G);
-      const int cl = complete ? cta : split_owner(ibase + nch - 1, U, G);
-      auto sum_rows = [&](int ridx, int nb, float (&acc)[16]) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        for (int cc = cf; cc <= cl; ++cc) {
-          const int slot = ((U * cc / G) / nch == item) ? 0 : 1;
-          const float* src = p.gpart + ((size_t)cc * 2 + slot) * p.slot_floats +
-                             (size_t)ridx * npad + nb;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + j);
-        }
-      };
-      if (w13) {
-        if (set == 0) {   // warps 0-3: gate row m and up row m of the item
-          const float g13 = P.act_g13[a13];
-          const int i_out = rb * 128 + m;
-          for (int nb = 0; nb < npad; nb += 16) {
-            float gv[16], uv[16];
-            if (complete) {
-              uint32_t g[16], uu[16];
-              tmem_ld16(tbase + lane_off + kColD0 + nb, g);
-              tmem_ld16(tbase + lane_off + kColD1 + nb, uu);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                gv[j] = __uint_as_float(g[j]);
-                uv[j] = __uint_as_float(uu[j]);
-              }
-            } else {
-              sum_rows(m, nb, gv);
-              sum_rows(128 + m, nb, uv);
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = nb + j;
-              if (n < nv) {
-                const int pr = pair0 + n;
-                const float sc = g13 * P.xscale[P.pair_tok[pr]];
-                const float hv = silu_clamped_swiglu(gv[j] * sc, uv[j] * sc, p.limit);
-                p.h[(size_t)pr * p.I + i_out] = __float2half_rn(hv * P.pair_wscale[pr]);
-              }
-            }
-          }
-        }
-      } else {
-        const float oscale = __int_as_float(P.misc[3]) * p.inv_hscale;
-        for (int nb = 0; nb < npad; nb += 16) {
-          float dv[16];
-          if (complete) {
-            uint32_t dd[16];
-            tmem_ld16(tbase + lane_off + dcol + nb, dd);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dv[j] = __uint_as_float(dd[j]);
-          } else {
-            sum_rows(set * 128 + m, nb, dv);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = nb + j;
-            if (n < nv && row_ok)
-              p.out[(size_t)n * p.H + row] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(dv[j] * oscale));
-          }
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();   // accumulators read before the next segment's first MMA
-    ++seg;
   }
-  return ok;
 }
 
-__global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ DecodeArgs p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t mbar_full[kStages];
-  __shared__ __align__(8) uint64_t mbar_done[kStages];
-  __shared__ uint32_t tmem_slot;
-  __shared__ int s_flag;
+// The same conversion as convert_token, from the registers.
+__device__ void x_t1_convert(const DecodeArgs& p, const XRegs& r, char* dst, float* s_scale,
+                             float* s_dot) {
+  __shared__ float red_a[32], red_d[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  float amax = 0.f, dot = 0.f;
+#pragma unroll
+  for (int c = 0; c < kXChunks; ++c) {
+    const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
+    const uint32_t gw[4] = {r.g[c].x, r.g[c].y, r.g[c].z, r.g[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+      dot = fmaf(lo, __uint_as_float(gw[j] << 16), dot);
+      dot = fmaf(hi, __uint_as_float(gw[j] & 0xFFFF0000u), dot);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  if (lane == 0) {
+    red_a[warp] = amax;
+    red_d[warp] = dot;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float a = 0.f, d = 0.f;
+    for (int w = 0; w < nw; ++w) {   // fixed order: reproducible
+      a = fmaxf(a, red_a[w]);
+      d += red_d[w];
+    }
+    int ex = 0;
+    if (a > 0.f) {
+      frexpf(a, &ex);
+      ex -= 9;
+    }
+    *s_scale = ldexpf(1.f, ex);
+    *s_dot = d;
+  }
+  __syncthreads();
+  const float down = 1.f / *s_scale;
+#pragma unroll
+  for (int c = 0; c < kXChunks; ++c) {
+    const int e = (tid + c * blockDim.x) * 8;
+    if (e < p.H) {
+      const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * down,
+                                             __uint_as_float(w[j] & 0xFFFF0000u) * down);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(dst + act_byte(e)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  __syncthreads();
+}
+
+// -------------------------------------------------------------------- the GEMV phases
+// Where a phase reads its f16 activation rows (padded, `row` bytes each): row of pair q at
+// base + idx * row, with idx = token of q (by_token) or q - p0.
+struct Act {
+  const char* base;
+  size_t row;
+  int by_token;
+  int p0;
+};
+
+// Shape of a phase: U units of S steps; J units per segment.
+template <int MODE>
+__device__ __forceinline__ void phase_shape(const DecodeArgs& p, const Plan& P, int& U, int& S,
+                                            int& J) {
+  const int ksn = ((MODE == kW13 ? p.H : p.I) + kStepElems - 1) / kStepElems;
+  if (MODE == kW13) {
+    J = p.I;
+    U = P.misc[5] * J;
+    S = ksn;
+  } else if (MODE == kW2Rows) {
+    J = p.H / 2;
+    U = J;
+    S = P.misc[0] * ksn;
+  } else {
+    J = p.H / 2;
+    U = P.misc[5] * J;
+    S = ksn;
+  }
+}
+
+// Position of a warp in its phase: unit (seg, j), active expert a (W2 over all experts),
+// k-step ks within the current block. A block is a run of ksn steps over the same two
+// rows; the walk advances block by block, with no division after the start.
+struct Walk {
+  int seg, j, a, ks;
+};
+
+template <int MODE>
+__device__ __forceinline__ void walk_init(Walk& c, int g, int S, int J, int ksn) {
+  const int u = g / S, s = g - u * S;
+  c.seg = u / J;
+  c.j = u - c.seg * J;
+  c.a = MODE == kW2Rows ? s / ksn : 0;
+  c.ks = s - c.a * ksn;
+}
+
+template <int MODE>
+__device__ __forceinline__ void next_block(Walk& c, int J, int n_act) {
+  c.ks = 0;
+  if (MODE == kW2Rows) {
+    if (++c.a < n_act) return;
+    c.a = 0;
+  }
+  if (++c.j == J) {
+    c.j = 0;
+    ++c.seg;
+  }
+}
+
+// Expert of the rows a warp streams at position c (-1 = shared expert).
+template <int MODE>
+__device__ __forceinline__ int walk_expert(const Plan& P, const Walk& c) {
+  return P.act_expert[MODE == kW2Rows ? c.a : P.seg_act[c.seg]];
+}
+
+// Base addresses (element 0) of the two weight rows a warp streams at position c: codes
+// and block scales of row 0 (gate j / output row 2j) and row 1 (up j / output row 2j+1).
+struct Rows {
+  const uint8_t *c0, *c1, *s0, *s1;
+};
+
+template <int MODE>
+__device__ __forceinline__ Rows rows_at(const DecodeArgs& p, const Plan& P, const Walk& c) {
+  const int K = MODE == kW13 ? p.H : p.I;
+  const size_t rb = (size_t)K / 2, rs = (size_t)K / 16;
+  const int e = walk_expert<MODE>(P, c);
+  const uint8_t *cb, *sb;
+  size_t r0, r1;
+  if (MODE == kW13) {
+    const size_t nr = 2 * (size_t)p.I;
+    cb = e >= 0 ? p.w13 + (size_t)e * nr * rb : p.sh_w13;
+    sb = e >= 0 ? p.s13 + (size_t)e * nr * rs : p.sh_s13;
+    r0 = (size_t)c.j;
+    r1 = (size_t)p.I + c.j;
+  } else {
+    cb = e >= 0 ? p.w2 + (size_t)e * p.H * rb : p.sh_w2;
+    sb = e >= 0 ? p.s2 + (size_t)e * p.H * rs : p.sh_s2;
+    r0 = 2 * (size_t)c.j;
+    r1 = r0 + 1;
+  }
+  return Rows{cb + r0 * rb, cb + r1 * rb, sb + r0 * rs, sb + r1 * rs};
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"((int)pred)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.ca.shared.global [%0], [%1], 4;\n\t}" ::"r"(dst),
+      "l"(src), "r"((int)pred)
+      : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+// One step for one token: the lane's 32 elements of both rows against its 32 activations
+// at xp (one padded group: four 16-byte loads at fixed offsets), accumulated into a0 / a1.
+__device__ __forceinline__ void dot_step(const uint32_t (&w0)[16], const uint32_t (&w1)[16],
+                                         const float (&s)[4], const char* xp, float& a0,
+                                         float& a1) {
+  uint4 xv[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) xv[c] = *reinterpret_cast<const uint4*>(xp + 16 * c);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    uint32_t p0 = 0, p1 = 0;
+#pragma unroll
+    for (int c = 2 * b; c < 2 * b + 2; ++c) {
+      const uint32_t xw[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        p0 = hfma2(w0[4 * c + m], xw[m], p0);
+        p1 = hfma2(w1[4 * c + m], xw[m], p1);
+      }
+    }
+    a0 = fmaf(s[b], hsum2(p0), a0);
+    a1 = fmaf(s[2 + b], hsum2(p1), a1);
+  }
+}
+
+__device__ __forceinline__ void dequant_row(const uint4& q, uint32_t (&w)[16]) {
+  e2m1x8_to_f16x2x4(q.x, w[0], w[1], w[2], w[3]);
+  e2m1x8_to_f16x2x4(q.y, w[4], w[5], w[6], w[7]);
+  e2m1x8_to_f16x2x4(q.z, w[8], w[9], w[10], w[11]);
+  e2m1x8_to_f16x2x4(q.w, w[12], w[13], w[14], w[15]);
+}
+
+// Finish a unit: lane t (< nv) holds the totals of token slot t (t0: row 0 / gate,
+// t1: row 1 / up).
+template <int MODE>
+__device__ __forceinline__ void finish_unit(const DecodeArgs& p, const Plan& P, const Walk& c,
+                                            int lane, int nv, float t0, float t1) {
+  if (lane >= nv) return;
+  if (MODE == kW13) {
+    const int pr = P.seg_pair0[c.seg] + lane;
+    const float sc = P.act_g13[P.seg_act[c.seg]] * P.xscale[P.pair_tok[pr]];
+    const float hv = silu_clamped_swiglu(t0 * sc, t1 * sc, p.limit);
+    *reinterpret_cast<__half*>(reinterpret_cast<char*>(p.h) + (size_t)pr * decode_act_row_bytes(p.I) +
+                               act_byte(c.j)) = __float2half_rn(hv * P.pair_wscale[pr]);
+  } else if (MODE == kW2Rows) {
+    const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(t0 * os));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(t1 * os));
+    *reinterpret_cast<uint32_t*>(p.out + 2 * (size_t)c.j) = lo | (hi << 16);
+  } else {
+    const int pr = P.seg_pair0[c.seg] + lane;
+    *reinterpret_cast<float2*>(p.part + (size_t)pr * p.H + 2 * (size_t)c.j) =
+        make_float2(t0, t1);
+  }
+}
+
+// Cut of a phase's steps into warp ranges of equal cost. Steps are ordered segment-major,
+// JS per segment; with `weighted` a step of segment s costs step_cost(tokens of s), else 1.
+// Warp v's range starts at the first step whose cost start reaches floor(Ctot * v / NW),
+// evaluated as q * v + floor(r * v / NW) with Ctot = q * NW + r, so no 64-bit division is
+// needed (r * v < NW^2 <= 2^26).
+struct CostMap {
+  int JS, n_seg, NW, weighted, r;
+  long long TS, Ctot, q;
+
+  __device__ __forceinline__ void set_total(long long total) {
+    Ctot = total;
+    q = total / NW;
+    r = (int)(total - q * NW);
+  }
+  __device__ __forceinline__ long long cost_lo(int v) const {
+    return q * v + (int)((unsigned)(r * v) / (unsigned)NW);
+  }
+  // cost before step g
+  __device__ __forceinline__ long long cost_at(const Plan& P, int g) const {
+    if (!weighted) return g;
+    const int seg = g / JS, k = g - seg * JS;
+    return (long long)JS * P.seg_cp[seg] +
+           (long long)k * step_cost(P.seg_pair0[seg + 1] - P.seg_pair0[seg]);
+  }
+  // first step of warp v
+  __device__ int first_step(const Plan& P, int v) const {
+    if (v >= NW) return (int)TS;
+    const long long L = cost_lo(v);
+    if (!weighted) return (int)L;
+    int lo = 0, hi = n_seg;   // largest seg < n_seg with JS * cp[seg] <= L
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)JS * P.seg_cp[mid] <= L) lo = mid;
+      else hi = mid;
+    }
+    const int rem = (int)(L - (long long)JS * P.seg_cp[lo]);   // < JS * cost of one step
+    const int c = step_cost(P.seg_pair0[lo + 1] - P.seg_pair0[lo]);
+    const int k = (rem + c - 1) / c;
+    return k >= JS ? (lo + 1) * JS : lo * JS + k;
+  }
+  // the warp whose cost range holds cost C (0 <= C < Ctot): estimate, then correct
+  __device__ int owner(long long C) const {
+    int v = (int)((float)C * (float)NW / (float)Ctot);
+    v = v < 0 ? 0 : (v >= NW ? NW - 1 : v);
+    while (v + 1 < NW && cost_lo(v + 1) <= C) ++v;
+    while (v > 0 && cost_lo(v) > C) --v;
+    return v;
+  }
+};
+
+// A unit cut by a warp-range boundary (a warp has at most two: the first and the last
+// of its range). Its partial sums wait in registers until the warp's range is done.
+struct Split {
+  Walk c;
+  int u, nv;
+  float m0, m1;
+};
+
+// After the range: publish the partials (one fence for both), count arrivals, and let the
+// last warp to arrive at each split unit add all partials in warp order and finish it.
+template <int NT, int MODE>
+__device__ __noinline__ void finish_splits(const DecodeArgs& p, const Plan& P, const CostMap cm,
+                                          int S, int w, int g0, int n, const Split s0,
+                                          const Split s1) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const Split& q = i == 0 ? s0 : s1;
+    if (i < n && lane < q.nv) {
+      float* dst = p.gpart + ((size_t)w * 2 + (q.u == g0 / S ? 0 : 1)) * (2 * NT);
+      dst[lane] = q.m0;
+      dst[NT + lane] = q.m1;
+    }
+  }
+  __threadfence();
+  __syncwarp();
+#pragma unroll 1
+  for (int i = 0; i < n; ++i) {
+    const Split& q = i == 0 ? s0 : s1;
+    const int ub = q.u * S;
+    const int wf = cm.owner(cm.cost_at(P, ub)), wl = cm.owner(cm.cost_at(P, ub + S - 1));
+    int last = 0;
+    if (lane == 0) {
+      int nown = 1, next = cm.first_step(P, wf + 1);
+      for (int v = wf + 1; v <= wl; ++v) {
+        const int lo = next;
+        next = cm.first_step(P, v + 1);
+        nown += lo < next;
+      }
+      const int old = atomicAdd(p.cnt + wf, 1);
+      last = old == nown - 1;
+      if (last) p.cnt[wf] = 0;   // ready for the next use
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    float t0 = 0.f, t1 = 0.f;
+    if (lane < q.nv) {
+      int next = cm.first_step(P, wf);
+      for (int v = wf; v <= wl; ++v) {
+        const int vlo = next;
+        next = cm.first_step(P, v + 1);
+        if (vlo >= next) continue;   // empty range
+        const int vs = (q.u == vlo / S) ? 0 : 1;
+        const float* src = p.gpart + ((size_t)v * 2 + vs) * (2 * NT);
+        t0 += __ldcg(src + lane);
+        t1 += __ldcg(src + NT + lane);
+      }
+    }
+    finish_unit<MODE>(p, P, q.c, lane, q.nv, t0, t1);
+  }
+}
+
+// One phase over this warp's contiguous range of (unit, step) positions. The ranges are
+// cut to equal cost (steps of a segment with more tokens weigh more). The weight steps
+// stream through a ring of kDecodeDepth shared-memory slots private to the warp
+// (cp.async), so the loop body is not unrolled and the copies need no registers. start()
+// only issues the first copies: it runs before whatever the phase waits for (the
+// activations, the grid barrier), so the weight stream is already in flight when run()
+// begins. Lane addresses advance by constants within a block of ksn steps over the same
+// two rows and are recomputed only between blocks.
+template <int NT, int MODE>
+struct PhaseStream {
+  static constexpr int kWarps = Warps<NT>::value;
+  static constexpr int D = kDecodeDepth;
+  static constexpr bool kWeighted = NT > 1 && MODE != kW2Rows;
+  int S, J, K, ksn, w, lane, g0, g1, gi, n_act, nks, nks_s;
+  CostMap cm;
+  uint32_t ring;
+  Walk wi, wc;                       // issue and compute positions
+  const uint8_t *ic0, *ic1, *isp;    // lane addresses of the next step to issue
+
+  __device__ __forceinline__ void block_addr(const DecodeArgs& p, const Plan& P) {
+    const Rows R = rows_at<MODE>(p, P, wi);
+    ic0 = R.c0 + lane * 16 + wi.ks * 512;
+    ic1 = R.c1 + lane * 16 + wi.ks * 512;
+    isp = ((lane >> 4) ? R.s1 : R.s0) + (lane & 15) * 4 + wi.ks * 64;
+  }
+
+  // Copy one step into a ring slot: the lane's 16 code bytes of each row (its own 32
+  // elements) and 4 scale bytes (lanes 0-15 row 0, lanes 16-31 row 1). Slot layout: row 0
+  // codes [0, 512), row 1 codes [512, 1024), row 0 scales [1024, 1088), row 1 scales
+  // [1088, 1152). Lanes past the end of a short row copy nothing.
+  __device__ __forceinline__ void issue_next(const DecodeArgs& p, const Plan& P, uint32_t slot) {
+    if (wi.ks < nks) {
+      cp_async16(slot + lane * 16, ic0, true);
+      cp_async16(slot + 512 + lane * 16, ic1, true);
+    }
+    if (wi.ks < nks_s) cp_async4(slot + 1024 + (lane >> 4) * 64 + (lane & 15) * 4, isp, true);
+    ic0 += 512;
+    ic1 += 512;
+    isp += 64;
+    ++gi;
+    if (++wi.ks == ksn) {
+      next_block<MODE>(wi, J, n_act);
+      if (gi < g1) block_addr(p, P);
+    }
+  }
+
+  __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base) {
+    lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    int U;
+    phase_shape<MODE>(p, P, U, S, J);
+    n_act = P.misc[0];
+    cm.TS = (long long)U * S;
+    cm.JS = J * S;
+    cm.n_seg = P.misc[5];
+    cm.NW = gridDim.x * kWarps;
+    cm.weighted = kWeighted ? 1 : 0;
+    K = MODE == kW13 ? p.H : p.I;
+    ksn = (K + kStepElems - 1) / kStepElems;
+    // k-steps in which this lane has code bytes / scale bytes to copy
+    nks = K > lane * 32 ? (K - lane * 32 + kStepElems - 1) / kStepElems : 0;
+    const int e_s = (lane & 15) * 64;
+    nks_s = K > e_s ? (K - e_s + kStepElems - 1) / kStepElems : 0;
+    w = blockIdx.x * kWarps + warp;
+    ring = smem_u32(ring_base) + (uint32_t)(warp * D * kDecodeSlot);
+    g0 = g1 = gi = 0;
+    if (cm.TS == 0) return;
+    cm.set_total(kWeighted ? (long long)cm.JS * P.seg_cp[cm.n_seg] : cm.TS);
+    g0 = cm.first_step(P, w);
+    g1 = cm.first_step(P, w + 1);
+    gi = g0;
+    if (g0 >= g1) return;
+    walk_init<MODE>(wi, g0, S, J, ksn);
+    wc = wi;
+    block_addr(p, P);
+#pragma unroll 1
+    for (int d = 0; d < D; ++d) {
+      if (gi < g1) issue_next(p, P, ring + d * kDecodeSlot);
+      cp_commit();   // one group per slot, empty or not: the wait count stays uniform
+    }
+  }
+
+  __device__ void run(const DecodeArgs& p, const Plan& P, const Act A) {
+    if (g0 >= g1) return;
+    float acc0[NT], acc1[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc0[t] = acc1[t] = 0.f;
+    Split sp[2];
+    int n_split = 0;
+    const uint32_t ring_end = ring + D * kDecodeSlot;
+    uint32_t sa = ring;
+    const size_t lane_act = (size_t)lane * kActGroupBytes;
+    int pr0 = 0, nv = 0;
+    const char* xb = nullptr;   // one token: the lane's activation group at k = 0
+    bool blk = true;
+
+#pragma unroll 1
+    for (int g = g0; g < g1; ++g) {
+      cp_wait<D - 1>();   // this lane's copies of step g are done
+      __syncwarp();       // ... and every other lane's (the scale bytes are shared)
+      const uint32_t la = sa + lane * 16, ls = sa + 1024 + lane * 2;
+      const uint4 c0 = lds128(la), c1 = lds128(la + 512);
+      const uint32_t scw = lds_u16(ls) | (lds_u16(ls + 64) << 16);
+      __syncwarp();       // the slot is read before it is refilled
+      if (gi < g1) issue_next(p, P, sa);
+      cp_commit();
+      sa += kDecodeSlot;
+      if (sa == ring_end) sa = ring;
+
+      if (blk) {   // tokens of this block
+        if (MODE == kW2Rows) {
+          pr0 = wc.a;   // one token: pair index = active expert index
+          nv = 1;
+        } else {
+          pr0 = P.seg_pair0[wc.seg];
+          nv = P.seg_pair0[wc.seg + 1] - pr0;
+        }
+        if (NT == 1) {
+          const int idx = A.by_token ? P.pair_tok[pr0] : pr0 - A.p0;
+          xb = A.base + (size_t)idx * A.row + lane_act;
+        }
+        blk = false;
+      }
+      if (wc.ks < nks) {
+        uint32_t w0[16], w1[16];
+        dequant_row(c0, w0);
+        dequant_row(c1, w1);
+        const uint32_t s01 = e4m3x2_to_f16x2(scw & 0xFFFFu);
+        const uint32_t s23 = e4m3x2_to_f16x2(scw >> 16);
+        const __half2 h01 = *reinterpret_cast<const __half2*>(&s01);
+        const __half2 h23 = *reinterpret_cast<const __half2*>(&s23);
+        const float s[4] = {__low2float(h01), __high2float(h01), __low2float(h23),
+                            __high2float(h23)};
+        const size_t koff = (size_t)wc.ks * (kStepElems / 32 * kActGroupBytes);
+        if (NT == 1) {
+          dot_step(w0, w1, s, xb + koff, acc0[0], acc1[0]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t < nv) {
+              const int pr = pr0 + t;
+              const int idx = A.by_token ? P.pair_tok[pr] : pr - A.p0;
+              dot_step(w0, w1, s, A.base + (size_t)idx * A.row + lane_act + koff, acc0[t],
+                       acc1[t]);
+            }
+          }
+        }
+      }
+      const bool blk_end = wc.ks + 1 == ksn;
+      const bool unit_end = blk_end && (MODE != kW2Rows || wc.a == n_act - 1);
+      if (unit_end || g == g1 - 1) {
+        // ---- end of a unit (or of this warp's range): reduce across the warp
+        float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t < nv) {
+            const float v0 = warp_sum(acc0[t]), v1 = warp_sum(acc1[t]);
+            if (lane == t) {
+              m0 = v0;
+              m1 = v1;
+            }
+          }
+          acc0[t] = acc1[t] = 0.f;
+        }
+        const int u = wc.seg * J + wc.j;
+        if (u * S >= g0 && u * S + S <= g1) {
+          finish_unit<MODE>(p, P, wc, lane, nv, m0, m1);
+        } else {   // first or last unit of the range, shared with a neighbour warp
+          Split& q = n_split == 0 ? sp[0] : sp[1];
+          q.c = wc;
+          q.u = u;
+          q.nv = nv;
+          q.m0 = m0;
+          q.m1 = m1;
+          ++n_split;
+        }
+      }
+      if (blk_end) {
+        next_block<MODE>(wc, J, n_act);
+        blk = true;
+      } else {
+        ++wc.ks;
+      }
+    }
+    cp_wait<0>();
+    if (n_split) finish_splits<NT, MODE>(p, P, cm, S, w, g0, n_split, sp[0], sp[1]);
+  }
+};
+
+// CTA-wide copy of padded activation rows into shared memory: row r <- src(r), `row`
+// bytes each (a multiple of 16).
+template <typename SrcRow>
+__device__ void stage_rows(char* dst, int rows, size_t row, SrcRow src) {
+  const int gpr = (int)(row / 16);   // 16-byte granules per row
+  for (int i = threadIdx.x; i < rows * gpr; i += blockDim.x) {
+    const int r = i / gpr, g = i - r * gpr;
+    reinterpret_cast<uint4*>(dst + (size_t)r * row)[g] =
+        __ldcg(reinterpret_cast<const uint4*>(src(r)) + g);
+  }
+}
+
+// Activation rows this CTA's W13 / W2-segment range needs: pairs [pA, pB). Staged into
+// shared memory when they fit, else read from the global copy.
+template <int NT, int MODE>
+__device__ Act stage_segments(const DecodeArgs& p, const Plan& P, const PhaseStream<NT, MODE>& st,
+                              char* stage, size_t stage_cap) {
+  constexpr int kWarps = Warps<NT>::value;
+  const int K = MODE == kW13 ? p.H : p.I;
+  const size_t row = decode_act_row_bytes(K);
+  const Act g = MODE == kW13 ? Act{reinterpret_cast<const char*>(p.xf), row, 1, 0}
+                             : Act{reinterpret_cast<const char*>(p.h), row, 0, 0};
+  if (st.cm.TS == 0) return g;
+  const int lo = st.cm.first_step(P, blockIdx.x * kWarps);
+  const int hi = st.cm.first_step(P, (blockIdx.x + 1) * kWarps);
+  if (lo >= hi) return g;
+  const int sa = lo / st.cm.JS, sb = (hi - 1) / st.cm.JS;
+  const int pA = P.seg_pair0[sa], pB = P.seg_pair0[sb + 1];
+  if ((size_t)(pB - pA) * row > stage_cap) return g;
+  if (MODE == kW13)
+    stage_rows(stage, pB - pA, row, [&](int r) {
+      return reinterpret_cast<const char*>(p.xf) + (size_t)P.pair_tok[pA + r] * row;
+    });
+  else
+    stage_rows(stage, pB - pA, row, [&](int r) {
+      return reinterpret_cast<const char*>(p.h) + (size_t)(pA + r) * row;
+    });
+  return Act{stage, row, 0, pA};
+}
+
+template <int NT>
+__global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
+    k_decode(const __grid_constant__ DecodeArgs p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float s_scale, s_dot;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const DecodeSmem L(p.T, p.k, p.E, p.H, p.I, p.sh_g13 != nullptr);
-  unsigned char* sB = smem_raw;                                   // [2][kBTile]
   Plan P;
   P.act_expert = reinterpret_cast<int*>(smem_raw + L.act_expert);
   P.act_pair0 = reinterpret_cast<int*>(smem_raw + L.act_pair0);
@@ -664,102 +1079,151 @@ __global__ void __launch_bounds__(kDT, 1) k_decode(const __grid_constant__ Decod
   P.pair_wscale = reinterpret_cast<float*>(smem_raw + L.pair_wscale);
   P.xscale = reinterpret_cast<float*>(smem_raw + L.xscale);
   P.misc = reinterpret_cast<int*>(smem_raw + L.misc);
-  int* scratch = reinterpret_cast<int*>(smem_raw + L.scratch);
-
-  if (warp == 0) tmem_alloc(&tmem_slot, kDCols);
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(&mbar_full[st], kDT);
-      mbar_init(&mbar_done[st], 1);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_slot;
+  P.seg_act = reinterpret_cast<int*>(smem_raw + L.seg_act);
+  P.seg_pair0 = reinterpret_cast<int*>(smem_raw + L.seg_pair0);
+  P.seg_cp = reinterpret_cast<int*>(smem_raw + L.seg_cp);
+  P.tok_pairs = reinterpret_cast<int*>(smem_raw + L.tok_pairs);
+  char* stage = reinterpret_cast<char*>(smem_raw + L.stage);
+  unsigned char* ring = smem_raw + L.ring;
+  const size_t stage_cap = (size_t)p.smem_bytes - L.stage;
 
   griddep_launch_dependents();
   griddep_wait();   // routing results may come from the previous kernel
 
-  if (p.T == 1) build_plan_t1(p, P);
-  else build_plan(p, P, scratch);
-  const int n_act = P.misc[0];
-  const int n_routed = P.misc[2];
+  // barrier targets: the arrival counter as this launch began, rounded down to whole grids
+  __shared__ unsigned long long s_base;
+  if (tid == 0) s_base = ld_acquire64(p.bar) / gridDim.x * gridDim.x;
+  int n_bar = 0;
+  auto barrier = [&]() {
+    ++n_bar;
+    grid_sync(p.bar, s_base + (unsigned long long)n_bar * gridDim.x, p.err);
+  };
+
   const bool has_shared = p.sh_g13 != nullptr;
-  const bool private_x = decode_x_on_chip(p.T, p.H);
-  __half* xsrc = private_x ? reinterpret_cast<__half*>(smem_raw + L.xs) : p.xf;
+  const bool x_on_chip = decode_x_on_chip(p.T, p.H);
+  char* xs = x_on_chip ? reinterpret_cast<char*>(smem_raw + L.xs) : reinterpret_cast<char*>(p.xf);
+  const size_t xrow = decode_act_row_bytes(p.H);
+  XRegs xr;
+  if (NT == 1) x_t1_load(p, xr);   // before the weight stream
+
+  if (NT == 1) build_plan_t1(p, P);
+  else build_plan<NT>(p, P, reinterpret_cast<int*>(ring));
+  // weights do not depend on the activations: their first copies go out now
+  PhaseStream<NT, kW13> w13s;
+  w13s.start(p, P, ring);
+  const int n_routed = P.misc[2];
 
   // activations: every CTA converts all tokens into its shared memory (small T), or the
   // CTAs convert one token each into a shared global copy (larger T), then a grid barrier
-  for (int t = private_x ? 0 : (int)blockIdx.x; t < p.T; t += private_x ? 1 : (int)gridDim.x) {
-    convert_token(p, t, xsrc + (size_t)t * p.H, &s_scale, &s_dot);
+  if (NT == 1) {
+    x_t1_convert(p, xr, xs, &s_scale, &s_dot);
     if (tid == 0) {
-      if (private_x) {
-        P.xscale[t] = s_scale;
-        if (has_shared)
+      P.xscale[0] = s_scale;
+      if (has_shared)
+        P.pair_wscale[n_routed] = 1.f / (1.f + expf(-s_dot)) * __int_as_float(P.misc[4]) * p.hscale;
+    }
+  } else {
+    for (int t = x_on_chip ? 0 : (int)blockIdx.x; t < p.T; t += x_on_chip ? 1 : (int)gridDim.x) {
+      convert_token(p, t, xs + (size_t)t * xrow, &s_scale, &s_dot);
+      if (tid == 0) {
+        if (x_on_chip) {
+          P.xscale[t] = s_scale;
+          if (has_shared)
+            P.pair_wscale[P.act_pair0[n_routed] + t] =
+                1.f / (1.f + expf(-s_dot)) * __int_as_float(P.misc[4]) * p.hscale;
+        } else {
+          p.xscale_g[t] = s_scale;
+          p.xscale_g[p.T + t] = s_dot;   // gate dot products travel with the scales
+        }
+      }
+    }
+    if (!x_on_chip) {
+      barrier();
+      for (int t = tid; t < p.T; t += blockDim.x) {
+        P.xscale[t] = __ldcg(p.xscale_g + t);
+        if (has_shared) {
+          const float d = __ldcg(p.xscale_g + p.T + t);
           P.pair_wscale[P.act_pair0[n_routed] + t] =
-              1.f / (1.f + expf(-s_dot)) * __int_as_float(P.misc[4]) * p.hscale;
-      } else {
-        p.xscale_g[t] = s_scale;
-        p.xscale_g[p.T + t] = s_dot;   // gate dot products travel with the scales
+              1.f / (1.f + expf(-d)) * __int_as_float(P.misc[4]) * p.hscale;
+        }
       }
     }
   }
-  if (!private_x) {
-    grid_sync(p.bar, p.err);
-    for (int t = tid; t < p.T; t += blockDim.x) {
-      P.xscale[t] = __ldcg(p.xscale_g + t);
-      if (has_shared) {
-        const float d = __ldcg(p.xscale_g + p.T + t);
-        P.pair_wscale[P.act_pair0[n_routed] + t] =
-            1.f / (1.f + expf(-d)) * __int_as_float(P.misc[4]) * p.hscale;
+  __syncthreads();
+
+  // ---- W13 + SwiGLU
+  const Act a13 = x_on_chip ? Act{xs, xrow, 1, 0} : stage_segments(p, P, w13s, stage, stage_cap);
+  __syncthreads();
+  w13s.run(p, P, a13);
+  // the W2 weight copies go out before the grid barrier, the activations (h) after it
+  PhaseStream<NT, NT == 1 ? kW2Rows : kW2Seg> w2s;
+  w2s.start(p, P, ring);
+  barrier();
+
+  // ---- W2
+  if (NT == 1) {
+    if (P.misc[0] == 0) {   // no active expert: the layer output is zero
+      for (int r = blockIdx.x * blockDim.x + tid; r < p.H; r += gridDim.x * blockDim.x)
+        p.out[r] = 0;
+    }
+    // h rows straight from global memory (L1 / L2)
+    w2s.run(p, P, Act{reinterpret_cast<const char*>(p.h), decode_act_row_bytes(p.I), 0, 0});
+  } else {
+    const Act a2 = stage_segments(p, P, w2s, stage, stage_cap);
+    __syncthreads();
+    w2s.run(p, P, a2);
+    barrier();
+    // per-token sum of the pair results, in slot order (shared expert last)
+    const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
+    const int half = p.H / 2, kk = p.k + 1;
+    for (int i = blockIdx.x * blockDim.x + tid; i < p.T * half; i += gridDim.x * blockDim.x) {
+      const int t = i / half, r = 2 * (i - t * half);
+      float s0 = 0.f, s1 = 0.f;
+      for (int j = 0; j < kk; ++j) {
+        const int pr = P.tok_pairs[t * kk + j];
+        if (pr >= 0) {
+          const float2 v =
+              __ldcg(reinterpret_cast<const float2*>(p.part + (size_t)pr * p.H + r));
+          s0 += v.x;
+          s1 += v.y;
+        }
       }
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(s0 * os));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(s1 * os));
+      *reinterpret_cast<uint32_t*>(p.out + (size_t)t * p.H + r) = lo | (hi << 16);
     }
   }
-  __threadfence();
-  __syncthreads();
-
-  Pipe S;
-  S.full = mbar_full;
-  S.done = mbar_done;
-  for (int st = 0; st < kStages; ++st) S.uses[st] = 0;
-  S.n = 0;
-  bool ok = run_phase(p, P, tbase, sB, S, n_act, xsrc, &s_flag, true, private_x);
-  grid_sync(p.bar, p.err);
-  if (ok) ok = run_phase(p, P, tbase, sB, S, n_act, nullptr, &s_flag, false, private_x);
-  (void)ok;
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, kDCols);
 }
 
 }  // namespace
 
 DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid) {
-  int routed = T * k < E ? T * k : E;
+  const int routed = T * k < E ? T * k : E;
+  const int nt = decode_nt(T);
+  const size_t nw = (size_t)grid * decode_warps(T);
   max_act = routed + (shared ? 1 : 0);
   max_pairs = T * k + (shared ? T : 0);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   err = take(16);
   bar = take(16);
-  cnt13 = take(sizeof(int) * (size_t)max_act * (I / 128));
-  cnt2 = take(sizeof(int) * (size_t)(H / kRowsPerItem + 1));   // ceil(H / 256) items
-  xf = take(decode_x_on_chip(T, H) ? 16 : 2 * (size_t)T * H);   // shared f16 copy otherwise
+  cnt = take(sizeof(int) * nw);
+  xf = take(decode_x_on_chip(T, H) ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
   xscale = take(sizeof(float) * 2 * (size_t)T);
-  h = take(2 * (size_t)max_pairs * I);
-  gpart = take(sizeof(float) * (size_t)grid * 2 * kRowsPerItem * (size_t)((T + 15) & ~15));
+  h = take((size_t)max_pairs * decode_act_row_bytes(I));
+  gpart = take(sizeof(float) * nw * 2 * 2 * nt);
+  part = take(T > 1 ? sizeof(float) * (size_t)max_pairs * H : 16);
   total = o;
 }
 
 __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bool shared) {
   const int routed = T * k < E ? T * k : E;
+  const int nt = decode_nt(T);
   ma = routed + (shared ? 1 : 0);
   mp = T * k + (shared ? T : 0);
+  ms = ma + mp / nt + 1;   // bounds the sum over experts of ceil(pairs / nt)
   (void)I;
-  size_t o = (size_t)kStages * kBTile;   // activation tiles first (1024-byte aligned base)
+  size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = (o + bytes + 15) / 16 * 16; return at; };
   act_expert = take(4 * (size_t)ma);
   act_pair0 = take(4 * (size_t)(ma + 1));
@@ -768,9 +1232,18 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
   pair_wscale = take(4 * (size_t)(mp > ma ? mp : ma));
   xscale = take(4 * (size_t)T);
   misc = take(4 * 8);
-  scratch = take((size_t)E * 8 + 4 + (size_t)T * k * 9 + 16);
-  xs = take(decode_x_on_chip(T, H) ? 2 * (size_t)T * H : 0);   // f16 activations on chip
-  total = o;
+  seg_act = take(4 * (size_t)ms);
+  seg_pair0 = take(4 * (size_t)(ms + 1));
+  seg_cp = take(4 * (size_t)(ms + 1));
+  tok_pairs = take(4 * (size_t)T * (k + 1));
+  xs = take(decode_x_on_chip(T, H) ? (size_t)T * decode_act_row_bytes(H) : 0);   // x on chip
+  const size_t ring_bytes = (size_t)decode_warps(T) * kDecodeDepth * kDecodeSlot;
+  ring = take(ring_bytes);   // per-warp weight-step rings
+  stage = take(0);
+  // the plan's scratch (several tokens) lives in the rings and the staging area before
+  // either is used
+  const size_t scratch = T > 1 ? (size_t)E * 8 + 4 + (size_t)T * k * 9 + 16 : 0;
+  total = ring + (scratch > ring_bytes ? scratch : ring_bytes);
 }
 
 cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
@@ -782,9 +1255,9 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   const DecodeSmem SL(T, k, ex.E, ex.H, ex.I, shared);
   char* base = static_cast<char*>(ws);
 
-  // 2^S with 2^S * L^2 < 65504: |h| < L^2, so the scaled h stays a normal f16.
-  int S = 0;
-  while (S < 24 && (double)limit * limit * std::ldexp(1.0, S + 1) < 65504.0) ++S;
+  // 2^S with 2^S * L^2 <= 512: |h| < L^2, so every f16 block sum of W2 stays below 2^15.
+  int S = -40;
+  while (S < 24 && (double)limit * limit * std::ldexp(1.0, S + 1) <= 512.0) ++S;
   const float hscale = (float)std::ldexp(1.0, S);
 
   DecodeArgs a;
@@ -798,35 +1271,39 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   a.limit = limit; a.hscale = hscale; a.inv_hscale = 1.0f / hscale;
   a.out = out;
   a.err = reinterpret_cast<int*>(base + WL.err);
-  a.bar = reinterpret_cast<unsigned*>(base + WL.bar);
-  a.cnt13 = reinterpret_cast<int*>(base + WL.cnt13);
-  a.cnt2 = reinterpret_cast<int*>(base + WL.cnt2);
+  a.bar = reinterpret_cast<unsigned long long*>(base + WL.bar);
+  a.cnt = reinterpret_cast<int*>(base + WL.cnt);
   a.xf = reinterpret_cast<__half*>(base + WL.xf);
   a.xscale_g = reinterpret_cast<float*>(base + WL.xscale);
   a.h = reinterpret_cast<__half*>(base + WL.h);
   a.gpart = reinterpret_cast<float*>(base + WL.gpart);
-  a.slot_floats = kRowsPerItem * ((T + 15) & ~15);
+  a.part = reinterpret_cast<float*>(base + WL.part);
 
-  // one CTA per SM: the kernel is a cooperative persistent grid that owns the SM's
-  // tensor memory; a large shared-memory request keeps a second CTA off the SM
-  const size_t smem = SL.total > kDecodeMinSmem ? SL.total : kDecodeMinSmem;
+  // one CTA per SM: the kernel is a cooperative persistent grid
+  const size_t smem = SL.total > kDecodeSmem ? SL.total : kDecodeSmem;
+  a.smem_bytes = (int)smem;
+  const bool t1 = decode_nt(T) == 1;
+  const int vi = t1 ? 0 : 1;
   constexpr int kDevs = 64;
-  static size_t smem_set[kDevs] = {};
+  static size_t smem_set[kDevs][2] = {};
   static bool pdl_off[kDevs] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
-  if (smem > smem_set[dev]) {
-    err = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > smem_set[dev][vi]) {
+    err = t1 ? cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem)
+             : cudaFuncSetAttribute(k_decode<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
     if (err != cudaSuccess) return err;
-    smem_set[dev] = smem;
+    smem_set[dev][vi] = smem;
   }
   for (int attempt = 0; attempt < 2; ++attempt) {
     const bool pdl = !pdl_off[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDT);
+    cfg.blockDim = dim3(32 * decode_warps(T));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[2];
@@ -836,7 +1313,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl ? 2 : 1;
-    err = cudaLaunchKernelEx(&cfg, k_decode, a);
+    err = t1 ? cudaLaunchKernelEx(&cfg, k_decode<1>, a) : cudaLaunchKernelEx(&cfg, k_decode<8>, a);
     if (err == cudaSuccess || !pdl) return err;
     (void)cudaGetLastError();   // cooperative + programmatic serialization refused
     pdl_off[dev] = true;

@@ -10,10 +10,10 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxDecodeT = 64;
 constexpr int kMaxGrid = 512;          // upper bound on the split-K grid (CTAs)
-constexpr int kChunk = 128;            // reduction elements per chunk (64 packed bytes/row)
-constexpr int kGemvWarps = 8;          // warps per CTA of the decode kernel
 constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each CTA's smem up to this
-constexpr size_t kDecodeMinSmem = 120 * 1024;  // keeps the decode kernel at one CTA per SM
+constexpr size_t kDecodeSmem = 200 * 1024;     // decode shared memory (one CTA per SM)
+constexpr int kDecodeDepth = 8;                // decode: weight steps in flight per warp
+constexpr int kDecodeSlot = 1152;              // bytes of one step: 2 x 512 codes + 2 x 64 scales
 
 // Error word bits (workspace offset 0).
 constexpr int kErrBadExpert = 1;
@@ -27,20 +27,37 @@ __host__ __device__ inline bool decode_x_on_chip(int T, int H) {
   return (size_t)T * (size_t)H * 2 <= kDecodeXOnChip;
 }
 
+// Decode activation rows (x and h, f16) keep every group of 32 elements in 80 bytes (64 of
+// data, 16 of padding): a warp whose 32 lanes each read their own group then touches 32
+// distinct shared-memory banks in every quarter-warp phase.
+constexpr int kActGroupBytes = 80;
+__host__ __device__ inline size_t decode_act_row_bytes(int K) {
+  return (size_t)K / 32 * kActGroupBytes;
+}
+
+// Tokens per decode segment (a run of one expert's (token, expert) pairs whose partial sums
+// a warp keeps in registers): the single-token path is specialised.
+__host__ __device__ inline int decode_nt(int T) { return T == 1 ? 1 : 8; }
+// Warps per CTA of the decode kernel (the several-token variant needs more registers).
+__host__ __device__ inline int decode_warps(int T) { return T == 1 ? 16 : 8; }
+
 // Byte offsets of every region inside a decode workspace (global memory, caller-owned),
 // 256-byte aligned. grid = the number of CTAs of the decode kernel.
 struct DecodeLayout {
   int max_act = 0;     // active experts (routed, distinct) + shared
   int max_pairs = 0;   // (token, expert) pairs incl. the shared expert's T pairs
-  size_t err = 0, bar = 0, cnt13 = 0, cnt2 = 0, xf = 0, xscale = 0, h = 0, gpart = 0, total = 0;
+  size_t err = 0, bar = 0, cnt = 0, xf = 0, xscale = 0, h = 0, gpart = 0, part = 0, total = 0;
   DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid);
 };
 
 // Shared-memory carve-up of the decode kernel (same code on host and device).
 struct DecodeSmem {
-  int ma = 0, mp = 0;
+  int ma = 0, mp = 0, ms = 0;
   size_t act_expert = 0, act_pair0 = 0, act_g13 = 0, pair_tok = 0, pair_wscale = 0,
-         xscale = 0, misc = 0, scratch = 0, xs = 0, total = 0;
+         xscale = 0, misc = 0, seg_act = 0, seg_pair0 = 0, seg_cp = 0, tok_pairs = 0, xs = 0,
+         ring = 0,
+         stage = 0,
+         total = 0;   // total = minimum; the staging area grows into whatever is granted
   __host__ __device__ DecodeSmem(int T, int k, int E, int H, int I, bool shared);
 };
 

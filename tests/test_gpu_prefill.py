@@ -43,14 +43,19 @@ def test_prefill_matches_oracle(spec):
     assert_close(bf16_to_f64(y), ref, spec.name)
 
 
-def test_prefill_matches_decode_bitwise_close():
-    """The two paths compute the same layer: they agree within the tolerance."""
+def test_prefill_matches_decode():
+    """The two paths compute the same layer: each meets the bound against the oracle, so
+    the two bf16 outputs differ by at most twice it (one bf16 ulp of the largest output
+    already takes about 2^-8 * max|y|, close to the single bound)."""
     spec = LayerSpec("pd", seed=58, T=24, E=20, k=5, H=512, I=256, shared=True)
     layer = make_layer(spec)
     m = ftmoe()
     y, _, (x, idx, w, ex, sh) = _run_prefill(layer)
     yd = m.decode(x, idx, w, ex, sh)
-    assert_close(bf16_to_f64(y), bf16_to_f64(yd), "prefill vs decode")
+    ref, _, _ = om.moe_layer(layer.x, layer.logits, spec.k, layer, shared=layer.shared)
+    assert_close(bf16_to_f64(y), ref, "prefill")
+    assert_close(bf16_to_f64(yd), ref, "decode")
+    assert_close(bf16_to_f64(y), bf16_to_f64(yd), "prefill vs decode", scale=2.0)
 
 
 def test_prefill_deterministic():
