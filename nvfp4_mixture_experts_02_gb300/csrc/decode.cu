@@ -71,11 +71,11 @@ struct DecodeArgs {
   uint16_t* out;
   int* err;
   unsigned long long* bar;   // grid barrier: monotonic arrival counter
-  int* cnt;         // arrivals per split unit, indexed by the unit's first warp
   __half* xf;       // f16 activations, one shared copy (when they do not fit on chip)
   float* xscale_g;  // per-token activation scale and shared-gate dot (shared copy)
   __half* h;        // SwiGLU outputs [pairs][I]
-  float* gpart;     // partial sums of split units: [warp][2 slots][2 * NT]
+  float2* wpart;    // one token: per-unit W2 results of each CTA [CTA][row pairs][experts]
+  int wpart_rows;   // row pairs per CTA slice of wpart
   float* part;      // several tokens: W2 result per (pair, output row) [pairs][H]
   int smem_bytes;   // dynamic shared memory granted to each CTA
 };
@@ -142,7 +142,20 @@ struct Plan {
   int* seg_pair0;     // first pair of each segment; [n_seg] = n_pairs
   int* seg_cp;        // cost prefix: sum over earlier segments of the cost of one step
   int* tok_pairs;     // [T][k + 1]: pairs of each token in slot order, shared last, -1 = none
+  const uint8_t** act_ptr;   // [n_act][4]: W13 codes, W13 scales, W2 codes, W2 scales
 };
+
+// Weight base addresses of active expert i (expert e, -1 = shared).
+__device__ __forceinline__ void set_act_ptr(const DecodeArgs& p, const Plan& P, int i, int e) {
+  const size_t rb13 = (size_t)p.H / 2, rs13 = (size_t)p.H / 16;
+  const size_t rb2 = (size_t)p.I / 2, rs2 = (size_t)p.I / 16;
+  const size_t n13 = 2 * (size_t)p.I, n2 = (size_t)p.H;
+  const uint8_t** a = P.act_ptr + 4 * i;
+  a[0] = e >= 0 ? p.w13 + (size_t)e * n13 * rb13 : p.sh_w13;
+  a[1] = e >= 0 ? p.s13 + (size_t)e * n13 * rs13 : p.sh_s13;
+  a[2] = e >= 0 ? p.w2 + (size_t)e * n2 * rb2 : p.sh_w2;
+  a[3] = e >= 0 ? p.s2 + (size_t)e * n2 * rs2 : p.sh_s2;
+}
 
 __device__ int block_exclusive_scan(int v, int* tmp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -247,6 +260,7 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
     const int e = P.act_expert[i];
     const float g2 = e >= 0 ? __ldg(p.g2 + e) : __ldg(p.sh_g2);
     P.act_g13[i] = e >= 0 ? __ldg(p.g13 + e) : __ldg(p.sh_g13);
+    set_act_ptr(p, P, i, e);
     P.pair_wscale[i] = g2;   // temporary: W2 scale per active expert
     gmax = fmaxf(gmax, g2);
   }
@@ -370,6 +384,7 @@ __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
       P.pair_wscale[a] = w * (g2 / g2ref) * p.hscale;
       P.seg_act[a] = a;
       P.seg_pair0[a] = a;
+      set_act_ptr(p, P, a, e);
     }
     if (lane == 0) {
       int n_act = n_routed;
@@ -380,6 +395,7 @@ __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
         P.pair_tok[n_act] = 0;
         P.seg_act[n_act] = n_act;
         P.seg_pair0[n_act] = n_act;
+        set_act_ptr(p, P, n_act, -1);
         ++n_act;
       }
       P.act_pair0[n_act] = n_act;
@@ -548,102 +564,88 @@ struct Act {
   int p0;
 };
 
-// Shape of a phase: U units of S steps; J units per segment.
+// A unit is the work one warp does from start to finish: both rows of one W13 row pair
+// (gate j, up j) of one segment; one W2 row pair (2j, 2j+1) of one segment (several
+// tokens); or, for one token, one W2 row pair of one active expert. Its S steps cover
+// the reduction in pieces of 1024 elements. Units are numbered segment-major (W13, W2 of
+// several tokens: u = seg * J + j) or row-pair-major (W2 of one token: u = j * n_act + a).
 template <int MODE>
-__device__ __forceinline__ void phase_shape(const DecodeArgs& p, const Plan& P, int& U, int& S,
-                                            int& J) {
-  const int ksn = ((MODE == kW13 ? p.H : p.I) + kStepElems - 1) / kStepElems;
+__device__ __forceinline__ void phase_shape(const DecodeArgs& p, const Plan& P, int& U, int& J,
+                                            int& S) {
+  S = ((MODE == kW13 ? p.H : p.I) + kStepElems - 1) / kStepElems;
   if (MODE == kW13) {
     J = p.I;
     U = P.misc[5] * J;
-    S = ksn;
   } else if (MODE == kW2Rows) {
     J = p.H / 2;
-    U = J;
-    S = P.misc[0] * ksn;
+    U = J * P.misc[0];
   } else {
     J = p.H / 2;
     U = P.misc[5] * J;
-    S = ksn;
   }
 }
 
-// Position of a warp in its phase: unit (seg, j), active expert a (W2 over all experts),
-// k-step ks within the current block. A block is a run of ksn steps over the same two
-// rows; the walk advances block by block, with no division after the start.
-struct Walk {
-  int seg, j, a, ks;
+// Cut of a phase's units into CTA ranges of equal cost. With `weighted`, a unit of segment
+// s costs step_cost(tokens of s), else 1. CTA v's range starts at the first unit whose cost
+// start reaches floor(Ctot * v / G), evaluated as q * v + floor(r * v / G) with
+// Ctot = q * G + r, so no 64-bit division is needed (r * v < G^2).
+struct UnitMap {
+  int J, n_seg, G, weighted, r;
+  long long U, Ctot, q;
+
+  __device__ __forceinline__ void set_total(long long total) {
+    Ctot = total;
+    q = total / G;
+    r = (int)(total - q * G);
+  }
+  __device__ __forceinline__ long long cost_lo(int v) const {
+    return q * v + (int)((unsigned)(r * v) / (unsigned)G);
+  }
+  __device__ int first_unit(const Plan& P, int v) const {
+    if (v >= G) return (int)U;
+    const long long L = cost_lo(v);
+    if (!weighted) return (int)L;
+    int lo = 0, hi = n_seg;   // largest seg < n_seg with J * cp[seg] <= L
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)J * P.seg_cp[mid] <= L) lo = mid;
+      else hi = mid;
+    }
+    const int rem = (int)(L - (long long)J * P.seg_cp[lo]);
+    const int c = step_cost(P.seg_pair0[lo + 1] - P.seg_pair0[lo]);
+    const int k = (rem + c - 1) / c;
+    return k >= J ? (lo + 1) * J : lo * J + k;
+  }
 };
 
-template <int MODE>
-__device__ __forceinline__ void walk_init(Walk& c, int g, int S, int J, int ksn) {
-  const int u = g / S, s = g - u * S;
-  c.seg = u / J;
-  c.j = u - c.seg * J;
-  c.a = MODE == kW2Rows ? s / ksn : 0;
-  c.ks = s - c.a * ksn;
-}
-
-template <int MODE>
-__device__ __forceinline__ void next_block(Walk& c, int J, int n_act) {
-  c.ks = 0;
-  if (MODE == kW2Rows) {
-    if (++c.a < n_act) return;
-    c.a = 0;
+// This CTA's unit range [lo, hi) of a phase (the same on every thread).
+template <int NT, int MODE>
+__device__ void cta_units(const DecodeArgs& p, const Plan& P, int& lo, int& hi) {
+  int U, J, S;
+  phase_shape<MODE>(p, P, U, J, S);
+  if (MODE == kW2Rows) {   // whole row pairs per CTA, all experts of each
+    lo = (int)((long long)J * blockIdx.x / gridDim.x) * P.misc[0];
+    hi = (int)((long long)J * (blockIdx.x + 1) / gridDim.x) * P.misc[0];
+    return;
   }
-  if (++c.j == J) {
-    c.j = 0;
-    ++c.seg;
-  }
+  UnitMap m;
+  m.J = J;
+  m.n_seg = P.misc[5];
+  m.G = gridDim.x;
+  m.weighted = NT > 1;
+  m.U = U;
+  lo = hi = 0;
+  if (U == 0) return;
+  m.set_total(m.weighted ? (long long)J * P.seg_cp[m.n_seg] : (long long)U);
+  lo = m.first_unit(P, blockIdx.x);
+  hi = m.first_unit(P, blockIdx.x + 1);
 }
 
-// Expert of the rows a warp streams at position c (-1 = shared expert).
-template <int MODE>
-__device__ __forceinline__ int walk_expert(const Plan& P, const Walk& c) {
-  return P.act_expert[MODE == kW2Rows ? c.a : P.seg_act[c.seg]];
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-
-// Base addresses (element 0) of the two weight rows a warp streams at position c: codes
-// and block scales of row 0 (gate j / output row 2j) and row 1 (up j / output row 2j+1).
-struct Rows {
-  const uint8_t *c0, *c1, *s0, *s1;
-};
-
-template <int MODE>
-__device__ __forceinline__ Rows rows_at(const DecodeArgs& p, const Plan& P, const Walk& c) {
-  const int K = MODE == kW13 ? p.H : p.I;
-  const size_t rb = (size_t)K / 2, rs = (size_t)K / 16;
-  const int e = walk_expert<MODE>(P, c);
-  const uint8_t *cb, *sb;
-  size_t r0, r1;
-  if (MODE == kW13) {
-    const size_t nr = 2 * (size_t)p.I;
-    cb = e >= 0 ? p.w13 + (size_t)e * nr * rb : p.sh_w13;
-    sb = e >= 0 ? p.s13 + (size_t)e * nr * rs : p.sh_s13;
-    r0 = (size_t)c.j;
-    r1 = (size_t)p.I + c.j;
-  } else {
-    cb = e >= 0 ? p.w2 + (size_t)e * p.H * rb : p.sh_w2;
-    sb = e >= 0 ? p.s2 + (size_t)e * p.H * rs : p.sh_s2;
-    r0 = 2 * (size_t)c.j;
-    r1 = r0 + 1;
-  }
-  return Rows{cb + r0 * rb, cb + r1 * rb, sb + r0 * rs, sb + r1 * rs};
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
-      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
-      "l"(src), "r"((int)pred)
-      : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool pred) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
-      "@p cp.async.ca.shared.global [%0], [%1], 4;\n\t}" ::"r"(dst),
-      "l"(src), "r"((int)pred)
-      : "memory");
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -665,6 +667,19 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ int4 lds_i4(uint32_t a) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_i4(uint32_t a, int4 v) {
+  asm volatile("st.shared.v4.s32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 // One step for one token: the lane's 32 elements of both rows against its 32 activations
 // at xp (one padded group: four 16-byte loads at fixed offsets), accumulated into a0 / a1.
 __device__ __forceinline__ void dot_step(const uint32_t (&w0)[16], const uint32_t (&w1)[16],
@@ -697,267 +712,138 @@ __device__ __forceinline__ void dequant_row(const uint4& q, uint32_t (&w)[16]) {
   e2m1x8_to_f16x2x4(q.w, w[12], w[13], w[14], w[15]);
 }
 
-// Finish a unit: lane t (< nv) holds the totals of token slot t (t0: row 0 / gate,
-// t1: row 1 / up).
-template <int MODE>
-__device__ __forceinline__ void finish_unit(const DecodeArgs& p, const Plan& P, const Walk& c,
-                                            int lane, int nv, float t0, float t1) {
-  if (lane >= nv) return;
-  if (MODE == kW13) {
-    const int pr = P.seg_pair0[c.seg] + lane;
-    const float sc = P.act_g13[P.seg_act[c.seg]] * P.xscale[P.pair_tok[pr]];
-    const float hv = silu_clamped_swiglu(t0 * sc, t1 * sc, p.limit);
-    *reinterpret_cast<__half*>(reinterpret_cast<char*>(p.h) + (size_t)pr * decode_act_row_bytes(p.I) +
-                               act_byte(c.j)) = __float2half_rn(hv * P.pair_wscale[pr]);
-  } else if (MODE == kW2Rows) {
-    const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(t0 * os));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(t1 * os));
-    *reinterpret_cast<uint32_t*>(p.out + 2 * (size_t)c.j) = lo | (hi << 16);
-  } else {
-    const int pr = P.seg_pair0[c.seg] + lane;
-    *reinterpret_cast<float2*>(p.part + (size_t)pr * p.H + 2 * (size_t)c.j) =
-        make_float2(t0, t1);
-  }
-}
-
-// Cut of a phase's steps into warp ranges of equal cost. Steps are ordered segment-major,
-// JS per segment; with `weighted` a step of segment s costs step_cost(tokens of s), else 1.
-// Warp v's range starts at the first step whose cost start reaches floor(Ctot * v / NW),
-// evaluated as q * v + floor(r * v / NW) with Ctot = q * NW + r, so no 64-bit division is
-// needed (r * v < NW^2 <= 2^26).
-struct CostMap {
-  int JS, n_seg, NW, weighted, r;
-  long long TS, Ctot, q;
-
-  __device__ __forceinline__ void set_total(long long total) {
-    Ctot = total;
-    q = total / NW;
-    r = (int)(total - q * NW);
-  }
-  __device__ __forceinline__ long long cost_lo(int v) const {
-    return q * v + (int)((unsigned)(r * v) / (unsigned)NW);
-  }
-  // cost before step g
-  __device__ __forceinline__ long long cost_at(const Plan& P, int g) const {
-    if (!weighted) return g;
-    const int seg = g / JS, k = g - seg * JS;
-    return (long long)JS * P.seg_cp[seg] +
-           (long long)k * step_cost(P.seg_pair0[seg + 1] - P.seg_pair0[seg]);
-  }
-  // first step of warp v
-  __device__ int first_step(const Plan& P, int v) const {
-    if (v >= NW) return (int)TS;
-    const long long L = cost_lo(v);
-    if (!weighted) return (int)L;
-    int lo = 0, hi = n_seg;   // largest seg < n_seg with JS * cp[seg] <= L
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if ((long long)JS * P.seg_cp[mid] <= L) lo = mid;
-      else hi = mid;
-    }
-    const int rem = (int)(L - (long long)JS * P.seg_cp[lo]);   // < JS * cost of one step
-    const int c = step_cost(P.seg_pair0[lo + 1] - P.seg_pair0[lo]);
-    const int k = (rem + c - 1) / c;
-    return k >= JS ? (lo + 1) * JS : lo * JS + k;
-  }
-  // the warp whose cost range holds cost C (0 <= C < Ctot): estimate, then correct
-  __device__ int owner(long long C) const {
-    int v = (int)((float)C * (float)NW / (float)Ctot);
-    v = v < 0 ? 0 : (v >= NW ? NW - 1 : v);
-    while (v + 1 < NW && cost_lo(v + 1) <= C) ++v;
-    while (v > 0 && cost_lo(v) > C) --v;
-    return v;
-  }
-};
-
-// A unit cut by a warp-range boundary (a warp has at most two: the first and the last
-// of its range). Its partial sums wait in registers until the warp's range is done.
-struct Split {
-  Walk c;
-  int u, nv;
-  float m0, m1;
-};
-
-// After the range: publish the partials (one fence for both), count arrivals, and let the
-// last warp to arrive at each split unit add all partials in warp order and finish it.
-template <int NT, int MODE>
-__device__ __noinline__ void finish_splits(const DecodeArgs& p, const Plan& P, const CostMap cm,
-                                          int S, int w, int g0, int n, const Split s0,
-                                          const Split s1) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const Split& q = i == 0 ? s0 : s1;
-    if (i < n && lane < q.nv) {
-      float* dst = p.gpart + ((size_t)w * 2 + (q.u == g0 / S ? 0 : 1)) * (2 * NT);
-      dst[lane] = q.m0;
-      dst[NT + lane] = q.m1;
-    }
-  }
-  __threadfence();
-  __syncwarp();
-#pragma unroll 1
-  for (int i = 0; i < n; ++i) {
-    const Split& q = i == 0 ? s0 : s1;
-    const int ub = q.u * S;
-    const int wf = cm.owner(cm.cost_at(P, ub)), wl = cm.owner(cm.cost_at(P, ub + S - 1));
-    int last = 0;
-    if (lane == 0) {
-      int nown = 1, next = cm.first_step(P, wf + 1);
-      for (int v = wf + 1; v <= wl; ++v) {
-        const int lo = next;
-        next = cm.first_step(P, v + 1);
-        nown += lo < next;
-      }
-      const int old = atomicAdd(p.cnt + wf, 1);
-      last = old == nown - 1;
-      if (last) p.cnt[wf] = 0;   // ready for the next use
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    __threadfence();
-    float t0 = 0.f, t1 = 0.f;
-    if (lane < q.nv) {
-      int next = cm.first_step(P, wf);
-      for (int v = wf; v <= wl; ++v) {
-        const int vlo = next;
-        next = cm.first_step(P, v + 1);
-        if (vlo >= next) continue;   // empty range
-        const int vs = (q.u == vlo / S) ? 0 : 1;
-        const float* src = p.gpart + ((size_t)v * 2 + vs) * (2 * NT);
-        t0 += __ldcg(src + lane);
-        t1 += __ldcg(src + NT + lane);
-      }
-    }
-    finish_unit<MODE>(p, P, q.c, lane, q.nv, t0, t1);
-  }
-}
-
-// One phase over this warp's contiguous range of (unit, step) positions. The ranges are
-// cut to equal cost (steps of a segment with more tokens weigh more). The weight steps
-// stream through a ring of kDecodeDepth shared-memory slots private to the warp
-// (cp.async), so the loop body is not unrolled and the copies need no registers. start()
-// only issues the first copies: it runs before whatever the phase waits for (the
-// activations, the grid barrier), so the weight stream is already in flight when run()
-// begins. Lane addresses advance by constants within a block of ksn steps over the same
-// two rows and are recomputed only between blocks.
+// The weight stream of one phase for one warp. Units come from the CTA's dispenser (a
+// shared counter over the CTA's unit range), so warps that run ahead take more of them.
+// Steps stream through a ring of kDecodeDepth shared-memory slots private to the warp
+// (cp.async), each with a header naming its unit and k-step; the issue side runs up to
+// kDecodeDepth steps ahead of the compute side and crosses unit boundaries freely.
+// start() only issues the first copies: it runs before whatever the phase waits for (the
+// activations, the grid barrier), so the weight stream is in flight when run() begins.
 template <int NT, int MODE>
 struct PhaseStream {
-  static constexpr int kWarps = Warps<NT>::value;
   static constexpr int D = kDecodeDepth;
-  static constexpr bool kWeighted = NT > 1 && MODE != kW2Rows;
-  int S, J, K, ksn, w, lane, g0, g1, gi, n_act, nks, nks_s;
-  CostMap cm;
+  int J, S, K, I, lane, n_act, nks, nks_s, u_hi, n_issued;
+  int* disp;
   uint32_t ring;
-  Walk wi, wc;                       // issue and compute positions
-  const uint8_t *ic0, *ic1, *isp;    // lane addresses of the next step to issue
+  int iu, ij, iseg, ia, iks;          // unit being issued (iu < 0: none left)
+  const uint8_t *ic0, *ic1, *isp;    // lane addresses of its next step
 
-  __device__ __forceinline__ void block_addr(const DecodeArgs& p, const Plan& P) {
-    const Rows R = rows_at<MODE>(p, P, wi);
-    ic0 = R.c0 + lane * 16 + wi.ks * 512;
-    ic1 = R.c1 + lane * 16 + wi.ks * 512;
-    isp = ((lane >> 4) ? R.s1 : R.s0) + (lane & 15) * 4 + wi.ks * 64;
+  // next unit from the dispenser, and the lane addresses of its first step
+  __device__ __forceinline__ void next_unit(const Plan& P) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(disp, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= u_hi) {
+      iu = -1;
+      return;
+    }
+    iu = u;
+    iks = 0;
+    if (MODE == kW2Rows) {
+      ij = u / n_act;
+      ia = u - ij * n_act;
+      iseg = 0;
+    } else {
+      iseg = u / J;
+      ij = u - iseg * J;
+      ia = P.seg_act[iseg];
+    }
+    // rows: W13 gate j and up j; W2 output rows 2j and 2j + 1
+    const size_t rb = (size_t)K / 2, rs = (size_t)K / 16;
+    const size_t r0 = MODE == kW13 ? (size_t)ij : 2 * (size_t)ij;
+    const size_t r1 = MODE == kW13 ? r0 + (size_t)I : r0 + 1;
+    const int o = MODE == kW13 ? 0 : 2;
+    const uint8_t* cb = P.act_ptr[4 * ia + o];
+    const uint8_t* sb = P.act_ptr[4 * ia + o + 1];
+    ic0 = cb + r0 * rb + lane * 16;
+    ic1 = cb + r1 * rb + lane * 16;
+    isp = sb + ((lane >> 4) ? r1 : r0) * rs + (lane & 15) * 4;
   }
 
   // Copy one step into a ring slot: the lane's 16 code bytes of each row (its own 32
-  // elements) and 4 scale bytes (lanes 0-15 row 0, lanes 16-31 row 1). Slot layout: row 0
-  // codes [0, 512), row 1 codes [512, 1024), row 0 scales [1024, 1088), row 1 scales
-  // [1088, 1152). Lanes past the end of a short row copy nothing.
-  __device__ __forceinline__ void issue_next(const DecodeArgs& p, const Plan& P, uint32_t slot) {
-    if (wi.ks < nks) {
-      cp_async16(slot + lane * 16, ic0, true);
-      cp_async16(slot + 512 + lane * 16, ic1, true);
+  // elements) and 4 scale bytes (lanes 0-15 row 0, lanes 16-31 row 1), plus the header.
+  // Slot layout: row 0 codes [0, 512), row 1 codes [512, 1024), row 0 scales
+  // [1024, 1088), row 1 scales [1088, 1152), header [1152, 1168): unit coordinates.
+  // Lanes past the end of a short row copy nothing.
+  __device__ __forceinline__ void issue_next(const Plan& P, uint32_t slot) {
+    if (iks < nks) {
+      cp_async16(slot + lane * 16, ic0);
+      cp_async16(slot + 512 + lane * 16, ic1);
     }
-    if (wi.ks < nks_s) cp_async4(slot + 1024 + (lane >> 4) * 64 + (lane & 15) * 4, isp, true);
+    if (iks < nks_s) cp_async4(slot + 1024 + (lane >> 4) * 64 + (lane & 15) * 4, isp);
+    if (lane == 0) sts_i4(slot + 1152, make_int4(iseg, ij, ia, iks));
     ic0 += 512;
     ic1 += 512;
     isp += 64;
-    ++gi;
-    if (++wi.ks == ksn) {
-      next_block<MODE>(wi, J, n_act);
-      if (gi < g1) block_addr(p, P);
-    }
+    ++n_issued;
+    if (++iks == S) next_unit(P);
   }
 
-  __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base) {
+  __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base, int* dispenser,
+                        int unit_hi) {
     lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     int U;
-    phase_shape<MODE>(p, P, U, S, J);
+    phase_shape<MODE>(p, P, U, J, S);
+    I = p.I;
     n_act = P.misc[0];
-    cm.TS = (long long)U * S;
-    cm.JS = J * S;
-    cm.n_seg = P.misc[5];
-    cm.NW = gridDim.x * kWarps;
-    cm.weighted = kWeighted ? 1 : 0;
     K = MODE == kW13 ? p.H : p.I;
-    ksn = (K + kStepElems - 1) / kStepElems;
     // k-steps in which this lane has code bytes / scale bytes to copy
     nks = K > lane * 32 ? (K - lane * 32 + kStepElems - 1) / kStepElems : 0;
     const int e_s = (lane & 15) * 64;
     nks_s = K > e_s ? (K - e_s + kStepElems - 1) / kStepElems : 0;
-    w = blockIdx.x * kWarps + warp;
     ring = smem_u32(ring_base) + (uint32_t)(warp * D * kDecodeSlot);
-    g0 = g1 = gi = 0;
-    if (cm.TS == 0) return;
-    cm.set_total(kWeighted ? (long long)cm.JS * P.seg_cp[cm.n_seg] : cm.TS);
-    g0 = cm.first_step(P, w);
-    g1 = cm.first_step(P, w + 1);
-    gi = g0;
-    if (g0 >= g1) return;
-    walk_init<MODE>(wi, g0, S, J, ksn);
-    wc = wi;
-    block_addr(p, P);
+    disp = dispenser;
+    u_hi = unit_hi;
+    n_issued = 0;
+    next_unit(P);
 #pragma unroll 1
     for (int d = 0; d < D; ++d) {
-      if (gi < g1) issue_next(p, P, ring + d * kDecodeSlot);
+      if (iu >= 0) issue_next(P, ring + d * kDecodeSlot);
       cp_commit();   // one group per slot, empty or not: the wait count stays uniform
     }
   }
 
-  __device__ void run(const DecodeArgs& p, const Plan& P, const Act A) {
-    if (g0 >= g1) return;
-    float acc0[NT], acc1[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc0[t] = acc1[t] = 0.f;
-    Split sp[2];
-    int n_split = 0;
+  // wpart (one token, W2): per-unit results [row pair - j0][active expert] as float2
+  __device__ void run(const DecodeArgs& p, const Plan& P, const Act A, float2* wpart, int j0) {
     const uint32_t ring_end = ring + D * kDecodeSlot;
     uint32_t sa = ring;
     const size_t lane_act = (size_t)lane * kActGroupBytes;
+    float acc0[NT], acc1[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc0[t] = acc1[t] = 0.f;
     int pr0 = 0, nv = 0;
     const char* xb = nullptr;   // one token: the lane's activation group at k = 0
-    bool blk = true;
 
 #pragma unroll 1
-    for (int g = g0; g < g1; ++g) {
-      cp_wait<D - 1>();   // this lane's copies of step g are done
+    for (int n_done = 0; n_done < n_issued; ++n_done) {
+      cp_wait<D - 1>();   // this lane's copies of this step are done
       __syncwarp();       // ... and every other lane's (the scale bytes are shared)
       const uint32_t la = sa + lane * 16, ls = sa + 1024 + lane * 2;
       const uint4 c0 = lds128(la), c1 = lds128(la + 512);
       const uint32_t scw = lds_u16(ls) | (lds_u16(ls + 64) << 16);
+      const int4 hd = lds_i4(sa + 1152);   // seg, j, a, ks of this step
       __syncwarp();       // the slot is read before it is refilled
-      if (gi < g1) issue_next(p, P, sa);
+      if (iu >= 0) issue_next(P, sa);
       cp_commit();
       sa += kDecodeSlot;
       if (sa == ring_end) sa = ring;
 
-      if (blk) {   // tokens of this block
+      const int seg = hd.x, j = hd.y, a = hd.z, ks = hd.w;
+      if (ks == 0) {   // tokens of this unit
         if (MODE == kW2Rows) {
-          pr0 = wc.a;   // one token: pair index = active expert index
+          pr0 = a;   // one token: pair index = active expert index
           nv = 1;
         } else {
-          pr0 = P.seg_pair0[wc.seg];
-          nv = P.seg_pair0[wc.seg + 1] - pr0;
+          pr0 = P.seg_pair0[seg];
+          nv = P.seg_pair0[seg + 1] - pr0;
         }
         if (NT == 1) {
           const int idx = A.by_token ? P.pair_tok[pr0] : pr0 - A.p0;
           xb = A.base + (size_t)idx * A.row + lane_act;
         }
-        blk = false;
       }
-      if (wc.ks < nks) {
+      if (ks < nks) {
         uint32_t w0[16], w1[16];
         dequant_row(c0, w0);
         dequant_row(c1, w1);
@@ -967,7 +853,7 @@ struct PhaseStream {
         const __half2 h23 = *reinterpret_cast<const __half2*>(&s23);
         const float s[4] = {__low2float(h01), __high2float(h01), __low2float(h23),
                             __high2float(h23)};
-        const size_t koff = (size_t)wc.ks * (kStepElems / 32 * kActGroupBytes);
+        const size_t koff = (size_t)ks * (kStepElems / 32 * kActGroupBytes);
         if (NT == 1) {
           dot_step(w0, w1, s, xb + koff, acc0[0], acc1[0]);
         } else {
@@ -982,10 +868,8 @@ struct PhaseStream {
           }
         }
       }
-      const bool blk_end = wc.ks + 1 == ksn;
-      const bool unit_end = blk_end && (MODE != kW2Rows || wc.a == n_act - 1);
-      if (unit_end || g == g1 - 1) {
-        // ---- end of a unit (or of this warp's range): reduce across the warp
+      if (ks == S - 1) {
+        // ---- end of the unit: reduce across the warp, finish
         float m0 = 0.f, m1 = 0.f;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -998,28 +882,25 @@ struct PhaseStream {
           }
           acc0[t] = acc1[t] = 0.f;
         }
-        const int u = wc.seg * J + wc.j;
-        if (u * S >= g0 && u * S + S <= g1) {
-          finish_unit<MODE>(p, P, wc, lane, nv, m0, m1);
-        } else {   // first or last unit of the range, shared with a neighbour warp
-          Split& q = n_split == 0 ? sp[0] : sp[1];
-          q.c = wc;
-          q.u = u;
-          q.nv = nv;
-          q.m0 = m0;
-          q.m1 = m1;
-          ++n_split;
+        if (lane < nv) {
+          if (MODE == kW13) {
+            const int pr = pr0 + lane;
+            const float sc = P.act_g13[P.seg_act[seg]] * P.xscale[P.pair_tok[pr]];
+            const float hv = silu_clamped_swiglu(m0 * sc, m1 * sc, p.limit);
+            *reinterpret_cast<__half*>(reinterpret_cast<char*>(p.h) +
+                                       (size_t)pr * decode_act_row_bytes(p.I) + act_byte(j)) =
+                __float2half_rn(hv * P.pair_wscale[pr]);
+          } else if (MODE == kW2Rows) {
+            wpart[(j - j0) * n_act + a] = make_float2(m0, m1);
+          } else {
+            const int pr = pr0 + lane;
+            *reinterpret_cast<float2*>(p.part + (size_t)pr * p.H + 2 * (size_t)j) =
+                make_float2(m0, m1);
+          }
         }
-      }
-      if (blk_end) {
-        next_block<MODE>(wc, J, n_act);
-        blk = true;
-      } else {
-        ++wc.ks;
       }
     }
     cp_wait<0>();
-    if (n_split) finish_splits<NT, MODE>(p, P, cm, S, w, g0, n_split, sp[0], sp[1]);
   }
 };
 
@@ -1035,21 +916,18 @@ __device__ void stage_rows(char* dst, int rows, size_t row, SrcRow src) {
   }
 }
 
-// Activation rows this CTA's W13 / W2-segment range needs: pairs [pA, pB). Staged into
-// shared memory when they fit, else read from the global copy.
-template <int NT, int MODE>
-__device__ Act stage_segments(const DecodeArgs& p, const Plan& P, const PhaseStream<NT, MODE>& st,
-                              char* stage, size_t stage_cap) {
-  constexpr int kWarps = Warps<NT>::value;
+// Activation rows the units [lo, hi) of a segment-major phase need: pairs [pA, pB). Staged
+// into shared memory when they fit, else read from the global copy.
+template <int MODE>
+__device__ Act stage_segments(const DecodeArgs& p, const Plan& P, int lo, int hi, char* stage,
+                              size_t stage_cap) {
   const int K = MODE == kW13 ? p.H : p.I;
+  const int J = MODE == kW13 ? p.I : p.H / 2;
   const size_t row = decode_act_row_bytes(K);
   const Act g = MODE == kW13 ? Act{reinterpret_cast<const char*>(p.xf), row, 1, 0}
                              : Act{reinterpret_cast<const char*>(p.h), row, 0, 0};
-  if (st.cm.TS == 0) return g;
-  const int lo = st.cm.first_step(P, blockIdx.x * kWarps);
-  const int hi = st.cm.first_step(P, (blockIdx.x + 1) * kWarps);
   if (lo >= hi) return g;
-  const int sa = lo / st.cm.JS, sb = (hi - 1) / st.cm.JS;
+  const int sa = lo / J, sb = (hi - 1) / J;
   const int pA = P.seg_pair0[sa], pB = P.seg_pair0[sb + 1];
   if ((size_t)(pB - pA) * row > stage_cap) return g;
   if (MODE == kW13)
@@ -1068,6 +946,8 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
     k_decode(const __grid_constant__ DecodeArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float s_scale, s_dot;
+  __shared__ int s_range[4];   // this CTA's unit ranges: W13 [0, 1), W2 [2, 3)
+  __shared__ int s_disp[2];    // unit dispensers
 
   const int tid = threadIdx.x;
   const DecodeSmem L(p.T, p.k, p.E, p.H, p.I, p.sh_g13 != nullptr);
@@ -1083,6 +963,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   P.seg_pair0 = reinterpret_cast<int*>(smem_raw + L.seg_pair0);
   P.seg_cp = reinterpret_cast<int*>(smem_raw + L.seg_cp);
   P.tok_pairs = reinterpret_cast<int*>(smem_raw + L.tok_pairs);
+  P.act_ptr = reinterpret_cast<const uint8_t**>(smem_raw + L.act_ptr);
   char* stage = reinterpret_cast<char*>(smem_raw + L.stage);
   unsigned char* ring = smem_raw + L.ring;
   const size_t stage_cap = (size_t)p.smem_bytes - L.stage;
@@ -1108,9 +989,17 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
 
   if (NT == 1) build_plan_t1(p, P);
   else build_plan<NT>(p, P, reinterpret_cast<int*>(ring));
+  if (tid == 0) {
+    cta_units<NT, kW13>(p, P, s_range[0], s_range[1]);
+    if (NT == 1) cta_units<NT, kW2Rows>(p, P, s_range[2], s_range[3]);
+    else cta_units<NT, kW2Seg>(p, P, s_range[2], s_range[3]);
+    s_disp[0] = s_range[0];
+    s_disp[1] = s_range[2];
+  }
+  __syncthreads();
   // weights do not depend on the activations: their first copies go out now
   PhaseStream<NT, kW13> w13s;
-  w13s.start(p, P, ring);
+  w13s.start(p, P, ring, &s_disp[0], s_range[1]);
   const int n_routed = P.misc[2];
 
   // activations: every CTA converts all tokens into its shared memory (small T), or the
@@ -1152,26 +1041,41 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   __syncthreads();
 
   // ---- W13 + SwiGLU
-  const Act a13 = x_on_chip ? Act{xs, xrow, 1, 0} : stage_segments(p, P, w13s, stage, stage_cap);
+  const Act a13 = x_on_chip ? Act{xs, xrow, 1, 0}
+                            : stage_segments<kW13>(p, P, s_range[0], s_range[1], stage, stage_cap);
   __syncthreads();
-  w13s.run(p, P, a13);
+  w13s.run(p, P, a13, nullptr, 0);
   // the W2 weight copies go out before the grid barrier, the activations (h) after it
   PhaseStream<NT, NT == 1 ? kW2Rows : kW2Seg> w2s;
-  w2s.start(p, P, ring);
+  w2s.start(p, P, ring, &s_disp[1], s_range[3]);
   barrier();
 
   // ---- W2
   if (NT == 1) {
-    if (P.misc[0] == 0) {   // no active expert: the layer output is zero
-      for (int r = blockIdx.x * blockDim.x + tid; r < p.H; r += gridDim.x * blockDim.x)
-        p.out[r] = 0;
-    }
-    // h rows straight from global memory (L1 / L2)
-    w2s.run(p, P, Act{reinterpret_cast<const char*>(p.h), decode_act_row_bytes(p.I), 0, 0});
-  } else {
-    const Act a2 = stage_segments(p, P, w2s, stage, stage_cap);
+    // h rows straight from global memory (L1 / L2); per-unit results into shared memory,
+    // then each row pair's sum over the active experts in a fixed order
+    const int n_act = P.misc[0];
+    const int j0 = s_range[2] / max(n_act, 1), j1 = s_range[3] / max(n_act, 1);
+    float2* wpart = p.wpart + (size_t)blockIdx.x * p.wpart_rows * n_act;
+    w2s.run(p, P, Act{reinterpret_cast<const char*>(p.h), decode_act_row_bytes(p.I), 0, 0}, wpart,
+            j0);
     __syncthreads();
-    w2s.run(p, P, a2);
+    const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
+    for (int i = tid; i < 2 * (j1 - j0); i += blockDim.x) {
+      const int jj = i >> 1, r = i & 1;
+      float v = 0.f;
+      for (int a = 0; a < n_act; ++a) {
+        const float2 q = __ldcg(wpart + jj * n_act + a);
+        v += r ? q.y : q.x;
+      }
+      p.out[2 * (size_t)(j0 + jj) + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v * os));
+    }
+    if (n_act == 0)   // no active expert: the layer output is zero
+      for (int r = blockIdx.x * blockDim.x + tid; r < p.H; r += gridDim.x * blockDim.x) p.out[r] = 0;
+  } else {
+    const Act a2 = stage_segments<kW2Seg>(p, P, s_range[2], s_range[3], stage, stage_cap);
+    __syncthreads();
+    w2s.run(p, P, a2, nullptr, 0);
     barrier();
     // per-token sum of the pair results, in slot order (shared expert last)
     const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
@@ -1199,19 +1103,17 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
 
 DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid) {
   const int routed = T * k < E ? T * k : E;
-  const int nt = decode_nt(T);
-  const size_t nw = (size_t)grid * decode_warps(T);
   max_act = routed + (shared ? 1 : 0);
   max_pairs = T * k + (shared ? T : 0);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   err = take(16);
   bar = take(16);
-  cnt = take(sizeof(int) * nw);
   xf = take(decode_x_on_chip(T, H) ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
   xscale = take(sizeof(float) * 2 * (size_t)T);
   h = take((size_t)max_pairs * decode_act_row_bytes(I));
-  gpart = take(sizeof(float) * nw * 2 * 2 * nt);
+  wpart_rows = (H / 2 + grid - 1) / grid;
+  wpart = take(T == 1 ? sizeof(float2) * (size_t)grid * wpart_rows * max_act : 16);
   part = take(T > 1 ? sizeof(float) * (size_t)max_pairs * H : 16);
   total = o;
 }
@@ -1236,6 +1138,7 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
   seg_pair0 = take(4 * (size_t)(ms + 1));
   seg_cp = take(4 * (size_t)(ms + 1));
   tok_pairs = take(4 * (size_t)T * (k + 1));
+  act_ptr = take(8 * 4 * (size_t)ma);
   xs = take(decode_x_on_chip(T, H) ? (size_t)T * decode_act_row_bytes(H) : 0);   // x on chip
   const size_t ring_bytes = (size_t)decode_warps(T) * kDecodeDepth * kDecodeSlot;
   ring = take(ring_bytes);   // per-warp weight-step rings
@@ -1272,11 +1175,11 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   a.out = out;
   a.err = reinterpret_cast<int*>(base + WL.err);
   a.bar = reinterpret_cast<unsigned long long*>(base + WL.bar);
-  a.cnt = reinterpret_cast<int*>(base + WL.cnt);
   a.xf = reinterpret_cast<__half*>(base + WL.xf);
   a.xscale_g = reinterpret_cast<float*>(base + WL.xscale);
   a.h = reinterpret_cast<__half*>(base + WL.h);
-  a.gpart = reinterpret_cast<float*>(base + WL.gpart);
+  a.wpart = reinterpret_cast<float2*>(base + WL.wpart);
+  a.wpart_rows = WL.wpart_rows;
   a.part = reinterpret_cast<float*>(base + WL.part);
 
   // one CTA per SM: the kernel is a cooperative persistent grid

@@ -13,7 +13,7 @@ constexpr int kMaxGrid = 512;          // upper bound on the split-K grid (CTAs)
 constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each CTA's smem up to this
 constexpr size_t kDecodeSmem = 200 * 1024;     // decode shared memory (one CTA per SM)
 constexpr int kDecodeDepth = 8;                // decode: weight steps in flight per warp
-constexpr int kDecodeSlot = 1152;              // bytes of one step: 2 x 512 codes + 2 x 64 scales
+constexpr int kDecodeSlot = 1168;              // one step: 2 x 512 codes, 2 x 64 scales, header
 
 // Error word bits (workspace offset 0).
 constexpr int kErrBadExpert = 1;
@@ -46,7 +46,8 @@ __host__ __device__ inline int decode_warps(int T) { return T == 1 ? 16 : 8; }
 struct DecodeLayout {
   int max_act = 0;     // active experts (routed, distinct) + shared
   int max_pairs = 0;   // (token, expert) pairs incl. the shared expert's T pairs
-  size_t err = 0, bar = 0, cnt = 0, xf = 0, xscale = 0, h = 0, gpart = 0, part = 0, total = 0;
+  int wpart_rows = 0;   // row pairs per CTA slice of the one-token W2 results
+  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, wpart = 0, part = 0, total = 0;
   DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid);
 };
 
@@ -54,8 +55,8 @@ struct DecodeLayout {
 struct DecodeSmem {
   int ma = 0, mp = 0, ms = 0;
   size_t act_expert = 0, act_pair0 = 0, act_g13 = 0, pair_tok = 0, pair_wscale = 0,
-         xscale = 0, misc = 0, seg_act = 0, seg_pair0 = 0, seg_cp = 0, tok_pairs = 0, xs = 0,
-         ring = 0,
+         xscale = 0, misc = 0, seg_act = 0, seg_pair0 = 0, seg_cp = 0, tok_pairs = 0, act_ptr = 0,
+         xs = 0, ring = 0,
          stage = 0,
          total = 0;   // total = minimum; the staging area grows into whatever is granted
   __host__ __device__ DecodeSmem(int T, int k, int E, int H, int I, bool shared);
