@@ -74,8 +74,8 @@ struct DecodeArgs {
   __half* xf;       // f16 activations, one shared copy (when they do not fit on chip)
   float* xscale_g;  // per-token activation scale and shared-gate dot (shared copy)
   __half* h;        // SwiGLU outputs [pairs][I]
-  float2* wpart;    // one token: per-unit W2 results of each CTA [CTA][row pairs][experts]
-  int wpart_rows;   // row pairs per CTA slice of wpart
+  float2* upart;    // one token: per-unit partial sums of each CTA [CTA][unit][8 lanes]
+  int upart_units;  // units per CTA slice of upart
   float* part;      // several tokens: W2 result per (pair, output row) [pairs][H]
   int smem_bytes;   // dynamic shared memory granted to each CTA
 };
@@ -91,12 +91,15 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
 
 // Grid barrier on a monotonic 64-bit arrival counter: barrier b of a launch completes when
 // the counter reaches base + (b + 1) * gridDim.x, base = its value when the launch began
-// (every launch adds gridDim.x per barrier, so base is a multiple of it). One release
-// add per CTA, no release step, no reset; the wait is bounded.
-__device__ void grid_sync(unsigned long long* bar, unsigned long long target, int* err) {
+// (every launch adds gridDim.x per barrier, so base is a multiple of it). Arrival (one
+// release add per CTA) and waiting are separate calls, so a CTA can start streaming the
+// next phase's weights in between; the wait is bounded.
+__device__ void grid_arrive(unsigned long long* bar) {
   __syncthreads();
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+}
+__device__ void grid_wait(unsigned long long* bar, unsigned long long target, int* err) {
   if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
     unsigned it = 0;
     while ((long long)(ld_acquire64(bar) - target) < 0) {
       if (++it > kSpinLimit) {
@@ -652,6 +655,7 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -714,19 +718,21 @@ __device__ __forceinline__ void dequant_row(const uint4& q, uint32_t (&w)[16]) {
 
 // The weight stream of one phase for one warp. Units come from the CTA's dispenser (a
 // shared counter over the CTA's unit range), so warps that run ahead take more of them.
-// Steps stream through a ring of kDecodeDepth shared-memory slots private to the warp
-// (cp.async), each with a header naming its unit and k-step; the issue side runs up to
-// kDecodeDepth steps ahead of the compute side and crosses unit boundaries freely.
-// start() only issues the first copies: it runs before whatever the phase waits for (the
-// activations, the grid barrier), so the weight stream is in flight when run() begins.
+// Steps stream through a ring of kDecodeDepth shared-memory slots private to the warp,
+// filled by per-lane cp.async (each lane copies its own 16 code bytes of both rows and 4
+// scale bytes; one commit group per slot), with a header naming the step's unit and
+// k-step. The issue side runs up to kDecodeDepth steps ahead of the compute side and
+// crosses unit boundaries freely. start() only issues the first copies: it runs before
+// whatever the phase waits for (the activations, the grid barrier), so the weights are in
+// flight when run() begins.
 template <int NT, int MODE>
 struct PhaseStream {
   static constexpr int D = kDecodeDepth;
   int J, S, K, I, lane, n_act, nks, nks_s, u_hi, n_issued;
   int* disp;
   uint32_t ring;
-  int iu, ij, iseg, ia, iks;          // unit being issued (iu < 0: none left)
-  const uint8_t *ic0, *ic1, *isp;    // lane addresses of its next step
+  int iu, ij, iseg, ia, iks;           // unit being issued (iu < 0: none left)
+  const uint8_t *ic0, *ic1, *isp;      // lane addresses of its next step
 
   // next unit from the dispenser, and the lane addresses of its first step
   __device__ __forceinline__ void next_unit(const Plan& P) {
@@ -763,15 +769,15 @@ struct PhaseStream {
   // Copy one step into a ring slot: the lane's 16 code bytes of each row (its own 32
   // elements) and 4 scale bytes (lanes 0-15 row 0, lanes 16-31 row 1), plus the header.
   // Slot layout: row 0 codes [0, 512), row 1 codes [512, 1024), row 0 scales
-  // [1024, 1088), row 1 scales [1088, 1152), header [1152, 1168): unit coordinates.
-  // Lanes past the end of a short row copy nothing.
+  // [1024, 1088), row 1 scales [1120, 1184), header [1216, 1232): seg, j, a, ks. Lanes
+  // past the end of a short row copy nothing.
   __device__ __forceinline__ void issue_next(const Plan& P, uint32_t slot) {
     if (iks < nks) {
       cp_async16(slot + lane * 16, ic0);
       cp_async16(slot + 512 + lane * 16, ic1);
     }
-    if (iks < nks_s) cp_async4(slot + 1024 + (lane >> 4) * 64 + (lane & 15) * 4, isp);
-    if (lane == 0) sts_i4(slot + 1152, make_int4(iseg, ij, ia, iks));
+    if (iks < nks_s) cp_async4(slot + 1024 + (lane >> 4) * 96 + (lane & 15) * 4, isp);
+    if (lane == 0) sts_i4(slot + 1216, make_int4(iseg, ij, ia, iks));
     ic0 += 512;
     ic1 += 512;
     isp += 64;
@@ -779,8 +785,8 @@ struct PhaseStream {
     if (++iks == S) next_unit(P);
   }
 
-  __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base, int* dispenser,
-                        int unit_hi) {
+  __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base,
+                        int* dispenser, int unit_hi) {
     lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     int U;
@@ -804,8 +810,10 @@ struct PhaseStream {
     }
   }
 
-  // wpart (one token, W2): per-unit results [row pair - j0][active expert] as float2
-  __device__ void run(const DecodeArgs& p, const Plan& P, const Act A, float2* wpart, int j0) {
+  // One token (NT == 1): a unit's lane sums are only folded to 8 partials, written to
+  // upart[(unit - u_lo) * 8 + lane] and finished by the whole CTA after the phase, so no
+  // warp waits on the reduction and the finish. Several tokens: reduce and finish here.
+  __device__ void run(const DecodeArgs& p, const Plan& P, const Act A, float2* upart, int u_lo) {
     const uint32_t ring_end = ring + D * kDecodeSlot;
     uint32_t sa = ring;
     const size_t lane_act = (size_t)lane * kActGroupBytes;
@@ -821,8 +829,8 @@ struct PhaseStream {
       __syncwarp();       // ... and every other lane's (the scale bytes are shared)
       const uint32_t la = sa + lane * 16, ls = sa + 1024 + lane * 2;
       const uint4 c0 = lds128(la), c1 = lds128(la + 512);
-      const uint32_t scw = lds_u16(ls) | (lds_u16(ls + 64) << 16);
-      const int4 hd = lds_i4(sa + 1152);   // seg, j, a, ks of this step
+      const uint32_t scw = lds_u16(ls) | (lds_u16(ls + 96) << 16);
+      const int4 hd = lds_i4(sa + 1216);   // seg, j, a, ks of this step
       __syncwarp();       // the slot is read before it is refilled
       if (iu >= 0) issue_next(P, sa);
       cp_commit();
@@ -868,7 +876,15 @@ struct PhaseStream {
           }
         }
       }
-      if (ks == S - 1) {
+      if (NT == 1 && ks == S - 1) {
+        float v0 = acc0[0] + __shfl_xor_sync(0xffffffffu, acc0[0], 16);
+        float v1 = acc1[0] + __shfl_xor_sync(0xffffffffu, acc1[0], 16);
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 8);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 8);
+        const int u = MODE == kW2Rows ? j * n_act + a : seg * J + j;
+        if (lane < 8) upart[(size_t)(u - u_lo) * 8 + lane] = make_float2(v0, v1);
+        acc0[0] = acc1[0] = 0.f;
+      } else if (ks == S - 1) {
         // ---- end of the unit: reduce across the warp, finish
         float m0 = 0.f, m1 = 0.f;
 #pragma unroll
@@ -890,8 +906,6 @@ struct PhaseStream {
             *reinterpret_cast<__half*>(reinterpret_cast<char*>(p.h) +
                                        (size_t)pr * decode_act_row_bytes(p.I) + act_byte(j)) =
                 __float2half_rn(hv * P.pair_wscale[pr]);
-          } else if (MODE == kW2Rows) {
-            wpart[(j - j0) * n_act + a] = make_float2(m0, m1);
           } else {
             const int pr = pr0 + lane;
             *reinterpret_cast<float2*>(p.part + (size_t)pr * p.H + 2 * (size_t)j) =
@@ -909,11 +923,13 @@ struct PhaseStream {
 template <typename SrcRow>
 __device__ void stage_rows(char* dst, int rows, size_t row, SrcRow src) {
   const int gpr = (int)(row / 16);   // 16-byte granules per row
+  const uint32_t d = smem_u32(dst);
   for (int i = threadIdx.x; i < rows * gpr; i += blockDim.x) {
     const int r = i / gpr, g = i - r * gpr;
-    reinterpret_cast<uint4*>(dst + (size_t)r * row)[g] =
-        __ldcg(reinterpret_cast<const uint4*>(src(r)) + g);
+    cp_async16(d + (uint32_t)((size_t)r * row) + 16 * g,
+               reinterpret_cast<const char*>(src(r)) + 16 * g);
   }
+  cp_wait_all();
 }
 
 // Activation rows the units [lo, hi) of a segment-major phase need: pairs [pA, pB). Staged
@@ -975,9 +991,10 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   __shared__ unsigned long long s_base;
   if (tid == 0) s_base = ld_acquire64(p.bar) / gridDim.x * gridDim.x;
   int n_bar = 0;
-  auto barrier = [&]() {
+  auto arrive = [&]() { grid_arrive(p.bar); };
+  auto wait = [&]() {
     ++n_bar;
-    grid_sync(p.bar, s_base + (unsigned long long)n_bar * gridDim.x, p.err);
+    grid_wait(p.bar, s_base + (unsigned long long)n_bar * gridDim.x, p.err);
   };
 
   const bool has_shared = p.sh_g13 != nullptr;
@@ -1027,7 +1044,8 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
       }
     }
     if (!x_on_chip) {
-      barrier();
+      arrive();
+      wait();
       for (int t = tid; t < p.T; t += blockDim.x) {
         P.xscale[t] = __ldcg(p.xscale_g + t);
         if (has_shared) {
@@ -1044,29 +1062,72 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   const Act a13 = x_on_chip ? Act{xs, xrow, 1, 0}
                             : stage_segments<kW13>(p, P, s_range[0], s_range[1], stage, stage_cap);
   __syncthreads();
-  w13s.run(p, P, a13, nullptr, 0);
-  // the W2 weight copies go out before the grid barrier, the activations (h) after it
+  // one token: the units' 8 partials in shared memory when they fit, else in the workspace
+  const size_t n13 = (size_t)(s_range[1] - s_range[0]) * 8 * sizeof(float2);
+  const bool up13_smem = NT == 1 && n13 <= stage_cap;
+  float2* upart = up13_smem ? reinterpret_cast<float2*>(stage)
+                            : p.upart + (size_t)blockIdx.x * p.upart_units * 8;
+  w13s.run(p, P, a13, upart, s_range[0]);
+  if (NT == 1) {   // finish this CTA's W13 units: 8 partials each, SwiGLU, h
+    __syncthreads();
+    const int J = p.I;
+    for (int i = tid; i < s_range[1] - s_range[0]; i += blockDim.x) {
+      const int u = s_range[0] + i, seg = u / J, j = u - seg * J;
+      float g = 0.f, up = 0.f;
+#pragma unroll
+      for (int l = 0; l < 8; ++l) {
+        const float2 q = up13_smem ? upart[(size_t)i * 8 + l] : __ldcg(upart + (size_t)i * 8 + l);
+        g += q.x;
+        up += q.y;
+      }
+      const int pr = P.seg_pair0[seg];
+      const float sc = P.act_g13[P.seg_act[seg]] * P.xscale[P.pair_tok[pr]];
+      const float hv = silu_clamped_swiglu(g * sc, up * sc, p.limit);
+      *reinterpret_cast<__half*>(reinterpret_cast<char*>(p.h) +
+                                 (size_t)pr * decode_act_row_bytes(p.I) + act_byte(j)) =
+          __float2half_rn(hv * P.pair_wscale[pr]);
+    }
+  }
+  // arrive at the grid barrier, send the W2 weight copies, then wait for the other CTAs
+  arrive();
   PhaseStream<NT, NT == 1 ? kW2Rows : kW2Seg> w2s;
   w2s.start(p, P, ring, &s_disp[1], s_range[3]);
-  barrier();
+  wait();
 
   // ---- W2
   if (NT == 1) {
-    // h rows straight from global memory (L1 / L2); per-unit results into shared memory,
-    // then each row pair's sum over the active experts in a fixed order
+    // the active experts' h rows in shared memory when they fit; per-unit partials after
+    // them (or in the workspace); each row pair's sum over the experts in a fixed order
     const int n_act = P.misc[0];
     const int j0 = s_range[2] / max(n_act, 1), j1 = s_range[3] / max(n_act, 1);
-    float2* wpart = p.wpart + (size_t)blockIdx.x * p.wpart_rows * n_act;
-    w2s.run(p, P, Act{reinterpret_cast<const char*>(p.h), decode_act_row_bytes(p.I), 0, 0}, wpart,
-            j0);
+    const size_t hrow = decode_act_row_bytes(p.I);
+    const size_t hbytes = (size_t)n_act * hrow;
+    Act a2{reinterpret_cast<const char*>(p.h), hrow, 0, 0};
+    size_t used = 0;
+    if (hbytes <= stage_cap) {
+      stage_rows(stage, n_act, hrow,
+                 [&](int r) { return reinterpret_cast<const char*>(p.h) + (size_t)r * hrow; });
+      a2 = Act{stage, hrow, 0, 0};
+      used = hbytes;
+    }
+    const size_t n2 = (size_t)(s_range[3] - s_range[2]) * 8 * sizeof(float2);
+    const bool up2_smem = used + n2 <= stage_cap;
+    float2* up2 = up2_smem ? reinterpret_cast<float2*>(stage + used)
+                           : p.upart + (size_t)blockIdx.x * p.upart_units * 8;
+    __syncthreads();
+    w2s.run(p, P, a2, up2, s_range[2]);
     __syncthreads();
     const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
     for (int i = tid; i < 2 * (j1 - j0); i += blockDim.x) {
       const int jj = i >> 1, r = i & 1;
       float v = 0.f;
       for (int a = 0; a < n_act; ++a) {
-        const float2 q = __ldcg(wpart + jj * n_act + a);
-        v += r ? q.y : q.x;
+        const float2* q = up2 + ((size_t)jj * n_act + a) * 8;
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+          const float2 t = up2_smem ? q[l] : __ldcg(q + l);
+          v += r ? t.y : t.x;
+        }
       }
       p.out[2 * (size_t)(j0 + jj) + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v * os));
     }
@@ -1076,7 +1137,8 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
     const Act a2 = stage_segments<kW2Seg>(p, P, s_range[2], s_range[3], stage, stage_cap);
     __syncthreads();
     w2s.run(p, P, a2, nullptr, 0);
-    barrier();
+    arrive();
+    wait();
     // per-token sum of the pair results, in slot order (shared expert last)
     const float os = __int_as_float(P.misc[3]) * p.inv_hscale;
     const int half = p.H / 2, kk = p.k + 1;
@@ -1112,8 +1174,11 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   xf = take(decode_x_on_chip(T, H) ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
   xscale = take(sizeof(float) * 2 * (size_t)T);
   h = take((size_t)max_pairs * decode_act_row_bytes(I));
-  wpart_rows = (H / 2 + grid - 1) / grid;
-  wpart = take(T == 1 ? sizeof(float2) * (size_t)grid * wpart_rows * max_act : 16);
+  // one token: per CTA, at most ceil(W13 units / grid) or ceil(row pairs / grid) * experts
+  const long long u13 = ((long long)max_act * I + grid - 1) / grid;
+  const long long u2 = (long long)((H / 2 + grid - 1) / grid) * max_act;
+  upart_units = (int)(u13 > u2 ? u13 : u2);
+  upart = take(T == 1 ? sizeof(float2) * 8 * (size_t)grid * upart_units : 16);
   part = take(T > 1 ? sizeof(float) * (size_t)max_pairs * H : 16);
   total = o;
 }
@@ -1178,8 +1243,8 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   a.xf = reinterpret_cast<__half*>(base + WL.xf);
   a.xscale_g = reinterpret_cast<float*>(base + WL.xscale);
   a.h = reinterpret_cast<__half*>(base + WL.h);
-  a.wpart = reinterpret_cast<float2*>(base + WL.wpart);
-  a.wpart_rows = WL.wpart_rows;
+  a.upart = reinterpret_cast<float2*>(base + WL.upart);
+  a.upart_units = WL.upart_units;
   a.part = reinterpret_cast<float*>(base + WL.part);
 
   // one CTA per SM: the kernel is a cooperative persistent grid

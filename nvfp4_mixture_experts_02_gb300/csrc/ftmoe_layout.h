@@ -12,8 +12,8 @@ constexpr int kMaxDecodeT = 64;
 constexpr int kMaxGrid = 512;          // upper bound on the split-K grid (CTAs)
 constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each CTA's smem up to this
 constexpr size_t kDecodeSmem = 200 * 1024;     // decode shared memory (one CTA per SM)
-constexpr int kDecodeDepth = 8;                // decode: weight steps in flight per warp
-constexpr int kDecodeSlot = 1168;              // one step: 2 x 512 codes, 2 x 64 scales, header
+constexpr int kDecodeDepth = 6;                // decode: weight steps in flight per warp
+constexpr int kDecodeSlot = 1232;              // one step: 2 x 512 codes, 2 x 96 scales, header
 
 // Error word bits (workspace offset 0).
 constexpr int kErrBadExpert = 1;
@@ -46,8 +46,8 @@ __host__ __device__ inline int decode_warps(int T) { return T == 1 ? 16 : 8; }
 struct DecodeLayout {
   int max_act = 0;     // active experts (routed, distinct) + shared
   int max_pairs = 0;   // (token, expert) pairs incl. the shared expert's T pairs
-  int wpart_rows = 0;   // row pairs per CTA slice of the one-token W2 results
-  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, wpart = 0, part = 0, total = 0;
+  int upart_units = 0;   // units per CTA slice of the one-token partial sums
+  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, upart = 0, part = 0, total = 0;
   DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid);
 };
 
