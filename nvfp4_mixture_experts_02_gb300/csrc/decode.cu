@@ -44,7 +44,7 @@ namespace {
 
 template <int NT>
 struct Warps {   // warps per CTA
-  static constexpr int value = NT == 1 ? 16 : 8;
+  static constexpr int value = 16;
 };
 constexpr int kStepElems = 1024;   // reduction elements of one warp step (32 per lane)
 constexpr uint32_t kSpinLimit = 1u << 26;
@@ -1262,7 +1262,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   if (smem > smem_set[dev][vi]) {
     err = t1 ? cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem)
-             : cudaFuncSetAttribute(k_decode<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+             : cudaFuncSetAttribute(k_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem);
     if (err != cudaSuccess) return err;
     smem_set[dev][vi] = smem;
@@ -1281,7 +1281,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl ? 2 : 1;
-    err = t1 ? cudaLaunchKernelEx(&cfg, k_decode<1>, a) : cudaLaunchKernelEx(&cfg, k_decode<8>, a);
+    err = t1 ? cudaLaunchKernelEx(&cfg, k_decode<1>, a) : cudaLaunchKernelEx(&cfg, k_decode<4>, a);
     if (err == cudaSuccess || !pdl) return err;
     (void)cudaGetLastError();   // cooperative + programmatic serialization refused
     pdl_off[dev] = true;

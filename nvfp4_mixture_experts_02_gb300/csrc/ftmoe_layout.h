@@ -11,7 +11,7 @@ constexpr int kMaxExperts = 4096;
 constexpr int kMaxDecodeT = 64;
 constexpr int kMaxGrid = 512;          // upper bound on the split-K grid (CTAs)
 constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each CTA's smem up to this
-constexpr size_t kDecodeSmem = 200 * 1024;     // decode shared memory (one CTA per SM)
+constexpr size_t kDecodeSmem = 224 * 1024;     // decode shared memory (one CTA per SM)
 constexpr int kDecodeDepth = 6;                // decode: weight steps in flight per warp
 constexpr int kDecodeSlot = 1232;              // one step: 2 x 512 codes, 2 x 96 scales, header
 
@@ -37,9 +37,9 @@ __host__ __device__ inline size_t decode_act_row_bytes(int K) {
 
 // Tokens per decode segment (a run of one expert's (token, expert) pairs whose partial sums
 // a warp keeps in registers): the single-token path is specialised.
-__host__ __device__ inline int decode_nt(int T) { return T == 1 ? 1 : 8; }
-// Warps per CTA of the decode kernel (the several-token variant needs more registers).
-__host__ __device__ inline int decode_warps(int T) { return T == 1 ? 16 : 8; }
+__host__ __device__ inline int decode_nt(int T) { return T == 1 ? 1 : 4; }
+// Warps per CTA of the decode kernel.
+__host__ __device__ inline int decode_warps(int T) { return T > 0 ? 16 : 0; }
 
 // Byte offsets of every region inside a decode workspace (global memory, caller-owned),
 // 256-byte aligned. grid = the number of CTAs of the decode kernel.
