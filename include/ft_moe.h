@@ -144,6 +144,30 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
                                uint16_t* out, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/*
+ * ft_moe_nvfp4_decode_noalloc — ft_moe_nvfp4_decode for callers that cannot allocate
+ * device memory: a host framework that owns the GPU's memory through its own pool, a
+ * latency-bound serving loop that must not call cudaMalloc / cudaFree (they can
+ * synchronise the device), or a plug-in handed only a stream and its tensors. The pages
+ * have no counterpart: this is a deployment variant of the decode entry point.
+ *   Arguments as for ft_moe_nvfp4_decode, without the workspace: the scratch is a fixed
+ *   16 MiB array inside the library, held on every GPU that loads it until the process
+ *   exits. Shapes whose decode scratch (ft_moe_workspace_bytes) exceeds it return
+ *   FT_ERR_WORKSPACE_TOO_SMALL; nothing is allocated, by this call or by any library
+ *   routine it uses.
+ *   The first call on a device does a one-time set-up there (the array's device address
+ *   and the SM count, with that device current); make that first call before any stream
+ *   capture. Each call clears the array's error word and barrier counter on `stream`
+ *   before its kernel; every call shares the array, so calls that overlap on the GPU
+ *   (other streams, other host threads) race: order them on one stream. Device-side
+ *   flags (bad expert ids, timeouts) are not reported by this variant.
+ */
+ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                                      const float* topk_w, int32_t k,
+                                      const ft_nvfp4_experts* ex,
+                                      const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                                      uint16_t* out, void* stream);
+
 /* Text of the last CUDA runtime error seen by this thread inside the library (the cause
  * behind an FT_ERR_CUDA); static storage, never NULL. */
 const char* ft_moe_last_cuda_error(void);

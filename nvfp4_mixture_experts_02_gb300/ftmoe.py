@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_UNSUPPORTED_SHAP
 
 EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_workspace_bytes",
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
-            "ft_moe_get_error", "ft_moe_last_cuda_error"]
+            "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc"]
 
 
 class FtError(RuntimeError):
@@ -66,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = layer
+    lib.ft_moe_nvfp4_decode_noalloc.restype = ctypes.c_int
+    lib.ft_moe_nvfp4_decode_noalloc.argtypes = layer[:9] + [vp]
     lib.ft_moe_last_cuda_error.restype = ctypes.c_char_p
     lib.ft_moe_get_error.restype = ctypes.c_int
     lib.ft_moe_get_error.argtypes = [vp, vp]
@@ -198,6 +200,23 @@ def decode(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, works
                                   stream=stream)
     return _layer(_LIB.ft_moe_nvfp4_decode, "ft_moe_nvfp4_decode", x, topk_idx, topk_w,
                   experts, shared, limit, out, workspace, stream)
+
+
+def decode_noalloc(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None,
+                   stream=None):
+    """ft_moe_nvfp4_decode_noalloc: decode with the library's fixed scratch array (no
+    workspace, no device allocation by the library)."""
+    T, k = x.shape[0], topk_idx.shape[1]
+    if out is None:
+        out = torch.empty((T, experts.H), dtype=torch.bfloat16, device=x.device)
+    ex = experts.cstruct()
+    sh = shared.cstruct() if shared is not None else None
+    st = _LIB.ft_moe_nvfp4_decode_noalloc(_ptr(x), T, _ptr(topk_idx), _ptr(topk_w), k,
+                                          ctypes.byref(ex),
+                                          ctypes.byref(sh) if sh is not None else None,
+                                          float(limit), _ptr(out), _stream(stream))
+    _check(st, "ft_moe_nvfp4_decode_noalloc")
+    return out
 
 
 def prefill(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, workspace=None,
