@@ -245,10 +245,11 @@ def run_ours(args, spec, rank, world, local):
     e2e = run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world)
 
     hbm, bf16, src = measured_peaks()
+    traffic = measured_traffic(spec.name)
     if prefill:
         achieved = flops_call / (dec_us * 1e-6) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
-                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": traffic,
                 "peak_source": src, "us_per_launch": round(dec_us, 3),
                 "kernel": "ft_moe_nvfp4_prefill (plan, activations, W13 and W2 tcgen05 "
                           "grouped GEMMs, reduce)",
@@ -256,7 +257,7 @@ def run_ours(args, spec, rank, world, local):
     else:
         achieved = bytes_call / (dec_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
                 "kernel": "k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in one launch)",
                 "us_per_launch": round(dec_us, 3)}
     res = {
@@ -265,7 +266,9 @@ def run_ours(args, spec, rank, world, local):
         "us_per_call": round(us_call, 3), "tokens_per_s": round(spec.T * steps_done * world /
                                                                  (step_ms * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights (e2m1 x e4m3 -> f16), f16 mma, f32 accumulate, bf16 in/out",
+        "dtype": ("nvfp4 weights (e2m1 x e4m3), f16 tcgen05 mma, f32 accumulate, bf16 in/out"
+                  if prefill else "nvfp4 weights (e2m1 x e4m3), f16x2 fma per 16-element block, "
+                  "f32 accumulate, bf16 in/out"),
         "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, N(0,1) bf16 x)",
         "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k, "H": spec.H,
                    "I": spec.I, "shared_expert": spec.shared, "instances": n_inst,
@@ -279,6 +282,26 @@ def run_ours(args, spec, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(spec, layers[:2], bytes_call)
     return res
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch from profiles/dram_traffic.md (an ncu capture), or None when
+    the table has no row for the workload or the kernel source changed since the capture."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    path = os.path.join(here, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) < 4 or cells[0] != workload:
+            continue
+        src = os.path.join(here, "nvfp4_mixture_experts_02_gb300", "csrc", cells[1])
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return int(cells[3]) if sha == cells[2] else None
+    return None
 
 
 def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
