@@ -1,8 +1,9 @@
 // Router: softmax -> top-k -> renormalise, one warp per token, any k <= 32 (the
 // non-power-of-2 top-k router of the FreeToken commit log, 512-expert entry).
 //
-// Each lane holds E/32 logits in registers. k rounds of a warp-wide argmax pick the
-// experts in descending logit order (equal logits -> lower expert index). The weights
+// Each lane holds E/32 logits in registers. k rounds of a warp-wide argmax (two warp
+// reductions per round) pick the experts in descending logit order (equal logits -> lower
+// expert index). The weights
 // are exp(l_j - l_0) / sum_i exp(l_i - l_0) over the kept experts, which is the
 // renormalised softmax.
 #include <cfloat>
@@ -18,6 +19,13 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
   // (v, e) ranks before (bv, be): larger logit, then lower expert id. be == INT_MAX means
   // "no candidate yet".
   return be == INT_MAX || v > bv || (v == bv && e < be);
+}
+
+// Order-preserving unsigned key of a float: larger float -> larger key, equal floats ->
+// equal keys (-0 is first made +0). Logits are not expected to be NaN.
+__device__ __forceinline__ unsigned fkey(float v) {
+  const unsigned b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 template <int VPL>
@@ -44,32 +52,29 @@ __global__ void __launch_bounds__(128) k_route(const float* __restrict__ logits,
     }
   }
 
+  // Each round: every lane's best untaken candidate (its slots are in increasing expert
+  // order, so a strict comparison keeps the lower id on equal logits), the largest key
+  // over the warp, then the lowest expert id among the lanes that hold it.
   float my_v = 0.f;
   int my_e = 0;
   for (int r = 0; r < k; ++r) {
     float bv = -FLT_MAX;
-    int be = INT_MAX;
+    int bi = -1;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      const int e = i * 32 + lane;
-      if (!((taken >> i) & 1u) && better(v[i], e, bv, be)) {
+      if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
         bv = v[i];
-        be = e;
+        bi = i;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (oe != INT_MAX && better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    // every lane now holds the same winner
+    const unsigned key = bi < 0 ? 0u : fkey(bv);
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+    const unsigned cand = (bi >= 0 && key == kmax) ? (unsigned)(bi * 32 + lane) : 0xffffffffu;
+    const int be = (int)__reduce_min_sync(0xffffffffu, cand);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const float wv = __shfl_sync(0xffffffffu, bv, be & 31);
     if (lane == r) {
-      my_v = bv;
+      my_v = wv;
       my_e = be;
     }
   }

@@ -44,6 +44,15 @@ def test_route_ties(E, k):
     _route_check(lg, k)
 
 
+@pytest.mark.parametrize("E,k", [(40, 6), (288, 8)])
+def test_route_signed_zero_ties(E, k):
+    """+0 and -0 logits are equal: they tie, and the lower expert id ranks first."""
+    rng = np.random.default_rng(7 * E)
+    lg = np.where(rng.random((16, E)) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+    lg[:, ::7] = -1.0   # some smaller logits among the zeros
+    _route_check(lg, k)
+
+
 def _run_decode(layer, limit=7.0):
     m = ftmoe()
     spec = layer.spec
