@@ -11,7 +11,8 @@
 //   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
 //                           part[pair], in slot order (deterministic), bf16 out
 //
-// k_pf_gemm is persistent (one CTA per SM, 8 warps). A work item is one token group of
+// k_pf_gemm is persistent (one CTA per SM, 8 producer warps and one MMA warp). A work
+// item is one token group of
 // one expert (up to 128 tokens, the MMA N) against 256 weight rows: for W13 the 128 gate
 // rows and the 128 matching up rows of a row block (two fp32 accumulators in tensor
 // memory, so SwiGLU pairs land in the same TMEM lane), for W2 two 128-row blocks of the
@@ -21,10 +22,12 @@
 // (tcgen05.st) as the MMA's A operand. The activations of the group (B operand) travel
 // through the same register pipeline into shared memory, in the canonical K-major
 // core-matrix layout. Every thread arrives on the stage's "full" mbarrier when its part of
-// a chunk is in place; one thread waits for all of them and issues tcgen05.mma (kind::f16,
+// a chunk is in place; the MMA warp waits for the stage and issues tcgen05.mma (kind::f16,
 // A from TMEM, B from shared memory, M=128, N = group size rounded up to 16, K=16 per
-// instruction), committing to the stage's "done" mbarrier. Four stages and no CTA-wide
-// barrier per chunk let the warps run ahead of the MMAs.
+// instruction), committing to the stage's "done" mbarrier. No producer ever waits on the
+// MMA issue itself, four stages and no CTA-wide barrier per chunk let the producers run
+// ahead of the MMAs, and the weight stream is read with an L2 evict-first policy so the
+// activation rows that the items of one group share stay in L2.
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -36,7 +39,8 @@ namespace ftmoe {
 
 namespace {
 
-constexpr int kPfThreads = 256;          // 8 warps: rows 0-127 of set 0 / set 1
+constexpr int kPfProducers = 256;        // 8 producer warps: rows 0-127 of set 0 / set 1
+constexpr int kPfThreads = kPfProducers + 32;   // + one warp that issues the MMAs
 constexpr int kPfN = 128;                // max tokens per group (MMA N)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
 constexpr int kPfStages = 4;              // pipeline stages = chunks in flight per thread
@@ -287,6 +291,21 @@ struct PfGemmArgs {
   int* err;
 };
 
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 16 bytes of the weight stream: no L1 allocation, 256-byte L2 fetches, evicted first.
+__device__ __forceinline__ uint4 ldg_weights16(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(ptr), "l"(pol));
+  return v;
+}
+
 template <bool kW13>
 __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant__ PfGemmArgs p) {
   extern __shared__ __align__(1024) unsigned char pf_smem[];
@@ -298,9 +317,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   __shared__ float s_xs[kPfN];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int set = warp >> 2;                 // row set 0 / 1
+  const bool producer = tid < kPfProducers;
+  const int set = (warp >> 2) & 1;           // row set 0 / 1 (producers)
   const int m = (warp & 3) * 32 + lane;      // row inside the set = TMEM lane
   unsigned char* sB = pf_smem;               // [kPfStages][kBTileBytes]
+  const uint64_t wpol = l2_evict_first_policy();
+  (void)lane;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -311,7 +333,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   }
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&mbar_full[s], kPfThreads);
+      mbar_init(&mbar_full[s], kPfProducers);
       mbar_init(&mbar_done[s], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -366,8 +388,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     uint4 qb[kPfStages][4];
     auto issue = [&](int d, int c) {
       if (row_ok) {
-        q[d][0] = ldg_stream16(wrow + (size_t)c * 32);
-        q[d][1] = ldg_stream16(wrow + (size_t)c * 32 + 16);
+        q[d][0] = ldg_weights16(wrow + (size_t)c * 32, wpol);
+        q[d][1] = ldg_weights16(wrow + (size_t)c * 32 + 16, wpol);
         sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)c * 4));
       } else {
         q[d][0] = q[d][1] = make_uint4(0, 0, 0, 0);
@@ -375,7 +397,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int i = tid + r * kPfThreads;
+        const int i = tid + r * kPfProducers;
         const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (i < npad * 8 && n < nv) {
@@ -385,10 +407,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         qb[d][r] = v;
       }
     };
+    const uint32_t idesc = idesc_f16(128, npad);
+    if (!producer) {
+      // ---- MMA warp: for each chunk, wait until every producer has filled the stage,
+      // issue its MMAs (lane 0) and commit them to the stage's "done" barrier
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = (int)(nprod % kPfStages);
+        ok = mbar_wait(&mbar_full[st], uses[st] & 1, p.err, kErrTimeout);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t b0 = smem_addr(sB + st * kBTileBytes);
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int ks = 0; ks < kPfKc / 16; ++ks)
+              mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
+                     tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
+                     smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&mbar_done[st]);
+        }
+        __syncwarp();
+        ++uses[st];
+        ++nprod;
+      }
+    }
+    if (producer) {
 #pragma unroll
     for (int d = 0; d < kPfStages; ++d)
       if (d < nchunks) issue(d, d);
-    const uint32_t idesc = idesc_f16(128, npad);
     for (int c0 = 0; c0 < nchunks && ok; c0 += kPfStages) {
 #pragma unroll
       for (int d = 0; d < kPfStages; ++d) {
@@ -404,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           unsigned char* bt = sB + st * kBTileBytes;
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
-            const int i = tid + rr * kPfThreads;
+            const int i = tid + rr * kPfProducers;
             if (i < npad * 8) {
               const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
               *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = qb[d][rr];
@@ -415,31 +462,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
           mbar_arrive(&mbar_full[st]);
-          if (tid == 0) {   // all rows of this chunk are in place: issue its MMAs
-            ok = mbar_wait(&mbar_full[st], uses[st] & 1, p.err, kErrTimeout);
-            tc_fence_after();
-            const uint32_t b0 = smem_addr(bt);
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-#pragma unroll
-              for (int ks = 0; ks < kPfKc / 16; ++ks)
-                mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
-                       tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
-                       smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&mbar_done[st]);
-          }
-          if (warp == 0) ok = __shfl_sync(0xffffffffu, ok, 0);   // keep warps converged
           ++uses[st];
           ++nprod;
         }
       }
+    }
     }
     // all MMAs of this item done -> read the accumulators
     for (int st = 0; st < kPfStages && ok; ++st)
       if (uses[st] > 0) ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
     ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
-    if (ok) {
+    if (ok && producer) {
       if (kW13) {
         // warps 0-3 and 4-7 share the lanes; split the columns in blocks of 16
         const float g13 = e >= 0 ? __ldg(p.g13 + e) : __ldg(p.sh_g13);
