@@ -655,7 +655,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -729,16 +728,19 @@ template <int NT, int MODE>
 struct PhaseStream {
   static constexpr int D = kDecodeDepth;
   int J, S, K, I, lane, n_act, nks, nks_s, u_hi, n_issued;
+  int pend;   // lane 0: the next unit, already taken from the dispenser
   int* disp;
   uint32_t ring;
   int iu, ij, iseg, ia, iks;           // unit being issued (iu < 0: none left)
   const uint8_t *ic0, *ic1, *isp;      // lane addresses of its next step
 
-  // next unit from the dispenser, and the lane addresses of its first step
+  // next unit from the dispenser, and the lane addresses of its first step. One grab is
+  // always in flight: the unit used now was taken by the previous call, and the one taken
+  // now is used by the next, so the atomic's latency is off the critical path (grabs are
+  // monotonic per CTA, so a warp that stops holds no unit anyone else needs).
   __device__ __forceinline__ void next_unit(const Plan& P) {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(disp, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
+    int u = __shfl_sync(0xffffffffu, pend, 0);
+    if (lane == 0 && u < u_hi) pend = atomicAdd(disp, 1);
     if (u >= u_hi) {
       iu = -1;
       return;
@@ -802,6 +804,7 @@ struct PhaseStream {
     disp = dispenser;
     u_hi = unit_hi;
     n_issued = 0;
+    pend = lane == 0 ? atomicAdd(disp, 1) : 0;
     next_unit(P);
 #pragma unroll 1
     for (int d = 0; d < D; ++d) {
@@ -920,16 +923,32 @@ struct PhaseStream {
 
 // CTA-wide copy of padded activation rows into shared memory: row r <- src(r), `row`
 // bytes each (a multiple of 16).
+// Plain loads, not cp.async, so that the weight rings' commit groups stay the only ones:
+// eight independent loads per thread are in flight before their stores.
 template <typename SrcRow>
 __device__ void stage_rows(char* dst, int rows, size_t row, SrcRow src) {
+  constexpr int B = 8;
   const int gpr = (int)(row / 16);   // 16-byte granules per row
-  const uint32_t d = smem_u32(dst);
-  for (int i = threadIdx.x; i < rows * gpr; i += blockDim.x) {
-    const int r = i / gpr, g = i - r * gpr;
-    cp_async16(d + (uint32_t)((size_t)r * row) + 16 * g,
-               reinterpret_cast<const char*>(src(r)) + 16 * g);
+  const int n = rows * gpr, step = (int)blockDim.x;
+  for (int i0 = threadIdx.x; i0 < n; i0 += B * step) {
+    uint4 v[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int i = i0 + b * step;
+      if (i < n) {
+        const int r = i / gpr, g = i - r * gpr;
+        v[b] = __ldcg(reinterpret_cast<const uint4*>(src(r)) + g);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int i = i0 + b * step;
+      if (i < n) {
+        const int r = i / gpr, g = i - r * gpr;
+        reinterpret_cast<uint4*>(dst + (size_t)r * row)[g] = v[b];
+      }
+    }
   }
-  cp_wait_all();
 }
 
 // Activation rows the units [lo, hi) of a segment-major phase need: pairs [pA, pB). Staged
