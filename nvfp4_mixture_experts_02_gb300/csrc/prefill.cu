@@ -44,6 +44,7 @@ constexpr int kPfThreads = kPfProducers + 32;   // + one warp that issues the MM
 constexpr int kPfN = 128;                // max tokens per group (MMA N)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
 constexpr int kPfStages = 4;              // pipeline stages = chunks in flight per thread
+constexpr int kPfBStages = 8;             // activation tiles in shared memory (2 x kPfStages)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 stages x 2 x 32 cols
 constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 16 KB per stage
@@ -291,6 +292,19 @@ struct PfGemmArgs {
   int* err;
 };
 
+// 16-byte cp.async to shared memory; src_bytes < 16 zero-fills the rest (0: no read).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   const bool producer = tid < kPfProducers;
   const int set = (warp >> 2) & 1;           // row set 0 / 1 (producers)
   const int m = (warp & 3) * 32 + lane;      // row inside the set = TMEM lane
-  unsigned char* sB = pf_smem;               // [kPfStages][kBTileBytes]
+  unsigned char* sB = pf_smem;               // [kPfBStages][kBTileBytes]
   const uint64_t wpol = l2_evict_first_policy();
   (void)lane;
 
@@ -382,10 +396,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     }
     __syncthreads();
 
-    // register pipeline: codes, scales and this thread's activation pieces, kPfStages deep
+    // register pipeline of the weight stream: codes and scales, kPfStages deep
     uint4 q[kPfStages][2];
     uint32_t sc[kPfStages];
-    uint4 qb[kPfStages][4];
     auto issue = [&](int d, int c) {
       if (row_ok) {
         q[d][0] = ldg_weights16(wrow + (size_t)c * 32, wpol);
@@ -395,17 +408,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         q[d][0] = q[d][1] = make_uint4(0, 0, 0, 0);
         sc[d] = 0;
       }
+    };
+    // the group's activation tile of chunk c straight into shared-memory stage bst
+    // (cp.async, no registers; padding rows n >= nv are zero-filled): one commit group
+    auto issue_b = [&](int c, int bst) {
+      const uint32_t bt = smem_addr(sB + bst * kBTileBytes);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = tid + r * kPfProducers;
-        const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (i < npad * 8 && n < nv) {
-          const size_t src_row = kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n);
-          v = __ldcg(reinterpret_cast<const uint4*>(p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j));
+        if (i < npad * 8) {
+          const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
+          const bool v = n < nv;
+          const size_t src_row = v ? (kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n)) : 0;
+          cp_async16_zfill(bt + btile_off(n, j),
+                           p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j, v ? 16u : 0u);
         }
-        qb[d][r] = v;
       }
+      cp_async_commit();
     };
     const uint32_t idesc = idesc_f16(128, npad);
     if (!producer) {
@@ -416,16 +435,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         ok = mbar_wait(&mbar_full[st], uses[st] & 1, p.err, kErrTimeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t b0 = smem_addr(sB + st * kBTileBytes);
+        {   // the whole warp passes the operands, one elected lane issues
+          const uint32_t b0 = smem_addr(sB + (int)(nprod % kPfBStages) * kBTileBytes);
 #pragma unroll
           for (int s = 0; s < 2; ++s)
 #pragma unroll
             for (int ks = 0; ks < kPfKc / 16; ++ks)
-              mma_ts(tbase + (s == 0 ? kColD0 : kColD1),
-                     tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
-                     smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(&mbar_done[st]);
+              mma_ts_warp(tbase + (s == 0 ? kColD0 : kColD1),
+                          tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
+                          smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+          mma_commit_warp(&mbar_done[st]);
         }
         __syncwarp();
         ++uses[st];
@@ -433,9 +452,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       }
     }
     if (producer) {
+    // Activation tiles run kPfStages chunks ahead in kPfBStages = 2 x kPfStages slots, so
+    // the slot a chunk fills was last read by the MMAs of the chunk kPfStages before the
+    // current one, whose completion the loop waits for anyway. Exactly one commit group
+    // per chunk (empty past the end), so "this chunk's tile landed" is a fixed wait count.
+    // Every earlier item's MMAs are complete here, so the first tiles can go out at once.
 #pragma unroll
-    for (int d = 0; d < kPfStages; ++d)
-      if (d < nchunks) issue(d, d);
+    for (int d = 0; d < kPfStages; ++d) {
+      if (d < nchunks) {
+        issue(d, d);
+        issue_b(d, (int)((nprod + d) % kPfBStages));
+      } else {
+        cp_async_commit();
+      }
+    }
     for (int c0 = 0; c0 < nchunks && ok; c0 += kPfStages) {
 #pragma unroll
       for (int d = 0; d < kPfStages; ++d) {
@@ -445,19 +475,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           if (uses[st] > 0)   // the MMAs that last read this stage are done
             ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
           tc_fence_after();
+          if (c + kPfStages < nchunks) issue_b(c + kPfStages, (int)((nprod + kPfStages) % kPfBStages));
+          else cp_async_commit();
           uint32_t r[32];
           dequant64(q[d][0], q[d][1], sc[d], r);
           tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
-          unsigned char* bt = sB + st * kBTileBytes;
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int i = tid + rr * kPfProducers;
-            if (i < npad * 8) {
-              const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
-              *reinterpret_cast<uint4*>(bt + btile_off(n, j)) = qb[d][rr];
-            }
-          }
           if (c + kPfStages < nchunks) issue(d, c + kPfStages);
+          cp_async_wait<kPfStages>();   // this chunk's activation tile has landed
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
@@ -632,7 +656,7 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
     cudaLaunchConfig_t cfg = pdl_cfg(dim3((T + 7) / 8), dim3(256), 0, stream, at);
     if ((err = cudaLaunchKernelEx(&cfg, k_pf_act, aa)) != cudaSuccess) return err;
   }
-  const size_t smem = (size_t)kPfStages * kBTileBytes;
+  const size_t smem = (size_t)kPfBStages * kBTileBytes;
   static bool attr_set[64] = {};
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -640,7 +664,7 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   if (!attr_set[dev]) {
     // one CTA per SM (the kernel takes all 512 TMEM columns): ask for enough shared memory
     // that a second CTA cannot be co-resident
-    const int want = 120 * 1024;
+    const int want = smem > 120 * 1024 ? (int)smem : 120 * 1024;
     if ((err = cudaFuncSetAttribute(k_pf_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     want)) != cudaSuccess)
       return err;
