@@ -367,8 +367,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   const int blocks = kW13 ? p.I / 128 : (p.H + 255) / 256;   // the last W2 block may be short
   const int n_items = n_groups * blocks;
   const size_t rowb = (size_t)K / 2, srowb = (size_t)K / 16;
-  uint32_t uses[kPfStages] = {0, 0, 0, 0};   // uses issued per stage (mbarrier parity)
-  uint32_t nprod = 0;                         // chunks produced; stage = nprod % kPfStages
+  // chunks produced so far: chunk n uses A stage n % kPfStages, whose barriers have then
+  // completed n / kPfStages phases (the parities follow from n, no per-stage counters:
+  // a dynamically indexed array would live in local memory and slow the MMA issue)
+  uint32_t nprod = 0;
   bool ok = true;
 
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -432,7 +434,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       // issue its MMAs (lane 0) and commit them to the stage's "done" barrier
       for (int c = 0; c < nchunks && ok; ++c) {
         const int st = (int)(nprod % kPfStages);
-        ok = mbar_wait(&mbar_full[st], uses[st] & 1, p.err, kErrTimeout);
+        ok = mbar_wait(&mbar_full[st], (nprod / kPfStages) & 1, p.err, kErrTimeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         tc_fence_after();
         {   // the whole warp passes the operands, one elected lane issues
@@ -447,7 +449,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           mma_commit_warp(&mbar_done[st]);
         }
         __syncwarp();
-        ++uses[st];
         ++nprod;
       }
     }
@@ -472,8 +473,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         const int c = c0 + d;
         if (c < nchunks && ok) {
           const int st = (int)(nprod % kPfStages);
-          if (uses[st] > 0)   // the MMAs that last read this stage are done
-            ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
+          if (nprod >= kPfStages)   // the MMAs that last read this stage are done
+            ok = mbar_wait(&mbar_done[st], (nprod / kPfStages - 1) & 1, p.err, kErrTimeout);
           tc_fence_after();
           if (c + kPfStages < nchunks) issue_b(c + kPfStages, (int)((nprod + kPfStages) % kPfBStages));
           else cp_async_commit();
@@ -486,7 +487,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
           mbar_arrive(&mbar_full[st]);
-          ++uses[st];
           ++nprod;
         }
       }
@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     }
     // all MMAs of this item done -> read the accumulators
     for (int st = 0; st < kPfStages && ok; ++st)
-      if (uses[st] > 0) ok = mbar_wait(&mbar_done[st], (uses[st] - 1) & 1, p.err, kErrTimeout);
+      if (nprod > (uint32_t)st)   // stage st was last used by chunk nprod-1-((nprod-1-st) % 4)
+        ok = mbar_wait(&mbar_done[st], ((nprod - 1 - st) / kPfStages) & 1, p.err, kErrTimeout);
     ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
     if (ok && producer) {
