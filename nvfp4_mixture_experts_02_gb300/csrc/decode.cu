@@ -353,48 +353,52 @@ __device__ void build_plan(const DecodeArgs& p, const Plan& P, int* scratch) {
 
 // The same plan for a single token, by warp 0 alone: the pairs are the valid slots in
 // slot order (k <= 32, one lane each), one segment per active expert.
-__device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
+// What warp 0 keeps in registers between the two halves of the one-token plan.
+struct PlanT1Regs {
+  float w, g2, g13, sg2, sg13;
+  int a, n_routed;
+  bool ok;
+};
+
+// One token, first half: the active experts, their weight pointers and the counts, which
+// is all the weight stream needs to start. The tensor scales are loaded here but first
+// used by finish_plan_t1, after the stream has started, so their latency is off the path
+// to the first weight copy.
+__device__ PlanT1Regs build_plan_t1(const DecodeArgs& p, const Plan& P) {
   const int tid = threadIdx.x, lane = tid & 31;
   const bool has_shared = p.sh_g13 != nullptr;
+  PlanT1Regs r{0.f, 0.f, 0.f, 0.f, 0.f, 0, 0, false};
   if (tid < 32) {
     const int k = p.k;
     const int e = lane < k ? p.topk_idx[lane] : -1;
-    const float w = lane < k ? p.topk_w[lane] : 0.f;
+    r.w = lane < k ? p.topk_w[lane] : 0.f;
     bool ok = lane < k && e >= 0 && e < p.E;
     for (int j = 0; j < k; ++j) {   // an id repeated in earlier slots is dropped
       const int ej = __shfl_sync(0xffffffffu, e, j);
       if (j < lane && ej == e) ok = false;
     }
     if (lane < k && !ok && blockIdx.x == 0) atomicOr(p.err, kErrBadExpert);
+    r.g2 = ok ? __ldg(p.g2 + e) : 0.f;
+    r.g13 = ok ? __ldg(p.g13 + e) : 0.f;
+    r.sg2 = has_shared ? __ldg(p.sh_g2) : 0.f;
+    r.sg13 = has_shared ? __ldg(p.sh_g13) : 0.f;
     const unsigned vm = __ballot_sync(0xffffffffu, ok);
-    const int a = __popc(vm & ((1u << lane) - 1u));
-    const int n_routed = __popc(vm);
-    const float g2 = ok ? __ldg(p.g2 + e) : 0.f;
-    const float g13 = ok ? __ldg(p.g13 + e) : 0.f;
-    const float sg2 = has_shared ? __ldg(p.sh_g2) : 0.f;
-    float gmax = fmaxf(g2, sg2), wmax = ok ? fmaxf(1.f, fabsf(w)) : 1.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-    }
-    const float g2ref = (gmax > 0.f ? gmax : 1.f) * wmax;
+    r.a = __popc(vm & ((1u << lane) - 1u));
+    r.n_routed = __popc(vm);
+    r.ok = ok;
     if (ok) {
-      P.act_expert[a] = e;
-      P.act_pair0[a] = a;
-      P.act_g13[a] = g13;
-      P.pair_tok[a] = 0;
-      P.pair_wscale[a] = w * (g2 / g2ref) * p.hscale;
-      P.seg_act[a] = a;
-      P.seg_pair0[a] = a;
-      set_act_ptr(p, P, a, e);
+      P.act_expert[r.a] = e;
+      P.act_pair0[r.a] = r.a;
+      P.pair_tok[r.a] = 0;
+      P.seg_act[r.a] = r.a;
+      P.seg_pair0[r.a] = r.a;
+      set_act_ptr(p, P, r.a, e);
     }
     if (lane == 0) {
-      int n_act = n_routed;
+      int n_act = r.n_routed;
       if (has_shared) {
         P.act_expert[n_act] = -1;
         P.act_pair0[n_act] = n_act;
-        P.act_g13[n_act] = __ldg(p.sh_g13);
         P.pair_tok[n_act] = 0;
         P.seg_act[n_act] = n_act;
         P.seg_pair0[n_act] = n_act;
@@ -405,13 +409,36 @@ __device__ void build_plan_t1(const DecodeArgs& p, const Plan& P) {
       P.seg_pair0[n_act] = n_act;
       P.misc[0] = n_act;
       P.misc[1] = n_act;
-      P.misc[2] = n_routed;
-      P.misc[3] = __float_as_int(g2ref);
-      P.misc[4] = __float_as_int(has_shared ? sg2 / g2ref : 0.f);
+      P.misc[2] = r.n_routed;
       P.misc[5] = n_act;
     }
   }
   __syncthreads();
+  return r;
+}
+
+// One token, second half (warp 0, no barrier): the scales. g2ref is the largest W2 tensor
+// scale times max(1, max |router weight|); read by the combines and, through misc[4], by
+// thread 0 when it finishes the shared-expert gate.
+__device__ void finish_plan_t1(const DecodeArgs& p, const Plan& P, const PlanT1Regs& r) {
+  const int lane = threadIdx.x & 31;
+  const bool has_shared = p.sh_g13 != nullptr;
+  float gmax = fmaxf(r.g2, r.sg2), wmax = r.ok ? fmaxf(1.f, fabsf(r.w)) : 1.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+  }
+  const float g2ref = (gmax > 0.f ? gmax : 1.f) * wmax;
+  if (r.ok) {
+    P.act_g13[r.a] = r.g13;
+    P.pair_wscale[r.a] = r.w * (r.g2 / g2ref) * p.hscale;
+  }
+  if (lane == 0) {
+    if (has_shared) P.act_g13[r.n_routed] = r.sg13;
+    P.misc[3] = __float_as_int(g2ref);
+    P.misc[4] = __float_as_int(has_shared ? r.sg2 / g2ref : 0.f);
+  }
 }
 
 // f16 activations of token t scaled by a power of two (max |x| in [256, 512)), stored as a
@@ -1023,7 +1050,8 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   XRegs xr;
   if (NT == 1) x_t1_load(p, xr);   // before the weight stream
 
-  if (NT == 1) build_plan_t1(p, P);
+  PlanT1Regs t1r{};
+  if (NT == 1) t1r = build_plan_t1(p, P);
   else build_plan<NT>(p, P, reinterpret_cast<int*>(ring));
   if (tid == 0) {
     cta_units<NT, kW13>(p, P, s_range[0], s_range[1]);
@@ -1036,6 +1064,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   // weights do not depend on the activations: their first copies go out now
   PhaseStream<NT, kW13> w13s;
   w13s.start(p, P, ring, &s_disp[0], s_range[1]);
+  if (NT == 1 && tid < 32) finish_plan_t1(p, P, t1r);
   const int n_routed = P.misc[2];
 
   // activations: every CTA converts all tokens into its shared memory (small T), or the
