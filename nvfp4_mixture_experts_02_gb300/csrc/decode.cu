@@ -1116,6 +1116,12 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   float2* upart = up13_smem ? reinterpret_cast<float2*>(stage)
                             : p.upart + (size_t)blockIdx.x * p.upart_units * 8;
   w13s.run(p, P, a13, upart, s_range[0]);
+  // One token: this warp's W13 units are done and its ring is empty, so its W2 weight
+  // copies go out now, while the CTA's other warps finish their last W13 units (the W2
+  // weights do not depend on h). Several tokens: after the arrival below (measured better
+  // there, the longer W13 phase leaves the copies less to hide).
+  PhaseStream<NT, NT == 1 ? kW2Rows : kW2Seg> w2s;
+  if (NT == 1) w2s.start(p, P, ring, &s_disp[1], s_range[3]);
   if (NT == 1) {   // finish this CTA's W13 units: 8 partials each, SwiGLU, h
     __syncthreads();
     const int J = p.I;
@@ -1136,10 +1142,9 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
           __float2half_rn(hv * P.pair_wscale[pr]);
     }
   }
-  // arrive at the grid barrier, send the W2 weight copies, then wait for the other CTAs
+  // h of this CTA is written: arrive at the grid barrier and wait for the other CTAs
   arrive();
-  PhaseStream<NT, NT == 1 ? kW2Rows : kW2Seg> w2s;
-  w2s.start(p, P, ring, &s_disp[1], s_range[3]);
+  if (NT > 1) w2s.start(p, P, ring, &s_disp[1], s_range[3]);
   wait();
 
   // ---- W2
