@@ -44,7 +44,7 @@ extern "C" {
 
 typedef enum {
   FT_OK = 0,
-  FT_ERR_INVALID_ARG = 1,       /* null pointer, k < 1, k > E, T < 1, bad limit, ... */
+  FT_ERR_INVALID_ARG = 1,       /* null pointer, k < 1, k > E, T < 0, bad limit, ... */
   FT_ERR_UNSUPPORTED_SHAPE = 2, /* H or I not a multiple of 128, k > 32, E > 4096, ...  */
   FT_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment stated below          */
   FT_ERR_WORKSPACE_TOO_SMALL = 4,
@@ -94,7 +94,8 @@ const char* ft_status_string(ft_status s);
  *             fp32 logits themselves, so the choice is exact.
  *   topk_w    float [T, k] out: softmax over all E renormalised over the kept k, i.e.
  *             exp(l_j - l_max) / sum over kept i of exp(l_i - l_max).
- *   1 <= k <= min(E, 32), 1 <= E <= 4096, T >= 1.
+ *   1 <= k <= min(E, 32), 1 <= E <= 4096, T >= 0. T = 0 (an empty batch) returns FT_OK
+ *   without reading or writing anything; the pointers may then be NULL.
  */
 ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                        int32_t* topk_idx, float* topk_w, void* stream);
@@ -102,7 +103,7 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
 /* Workspace bytes that decode (prefill = 0) or prefill (prefill = 1) needs for these
  * sizes on the current device; has_shared = 1 when a shared expert is passed. Without a
  * usable device the decode figure is an upper bound for any GPU. Returns 0 for invalid
- * sizes. */
+ * sizes and for T = 0 (an empty batch needs no workspace). */
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                               int32_t has_shared, int32_t prefill);
 
@@ -111,7 +112,9 @@ size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_
 ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * ft_moe_nvfp4_decode — the expert part of the layer for a decode batch (1 <= T <= 64).
+ * ft_moe_nvfp4_decode — the expert part of the layer for a decode batch (0 <= T <= 64).
+ *   T = 0 (an empty batch) returns FT_OK after the shape checks without reading or
+ *   writing anything; x, topk_idx, topk_w, out and workspace may then be NULL.
  *   x            bf16 [T, H] (16-byte aligned)
  *   topk_idx     int32 [T, k], topk_w float [T, k]: as written by ft_moe_route (any
  *                source is accepted; an id outside [0, E) raises FT_ERR_DEVICE_FLAG in the
@@ -133,7 +136,7 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
                               void* stream);
 
 /*
- * ft_moe_nvfp4_prefill — the same layer for a multi-token chunk (any T >= 1), run as
+ * ft_moe_nvfp4_prefill — the same layer for a multi-token chunk (any T >= 0), run as
  * grouped dense contractions: tokens are grouped by expert on the GPU, NVFP4 tiles are
  * dequantised to bf16 on chip and multiplied on the tensor cores. Arguments as for
  * decode, with workspace of at least ft_moe_workspace_bytes(T,k,E,H,I,sh!=0,1) bytes.

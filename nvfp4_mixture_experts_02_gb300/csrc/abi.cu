@@ -80,10 +80,11 @@ ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx
                            const void* ws) {
   ft_status st = check_experts(ex, sh);
   if (st != FT_OK) return st;
-  if (!x || !topk_idx || !topk_w || !out || !ws) return FT_ERR_INVALID_ARG;
-  if (T < 1 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
+  if (T < 0 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
   if (k > kMaxTopK) return FT_ERR_UNSUPPORTED_SHAPE;
   if (!(limit > 0.0f) || !(limit <= 128.0f)) return FT_ERR_INVALID_ARG;
+  if (T == 0) return FT_OK;   // an empty batch touches no buffer: the callers return at once
+  if (!x || !topk_idx || !topk_w || !out || !ws) return FT_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
       !aligned(ws, 256))
     return FT_ERR_MISALIGNED;
@@ -112,9 +113,10 @@ const char* ft_status_string(ft_status s) {
 
 ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                        int32_t* topk_idx, float* topk_w, void* stream) {
-  if (!logits || !topk_idx || !topk_w) return FT_ERR_INVALID_ARG;
-  if (T < 1 || E < 1 || k < 1 || k > E) return FT_ERR_INVALID_ARG;
+  if (T < 0 || E < 1 || k < 1 || k > E) return FT_ERR_INVALID_ARG;
   if (k > kMaxTopK || E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return FT_OK;   // empty batch: nothing to read or write
+  if (!logits || !topk_idx || !topk_w) return FT_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
     return FT_ERR_MISALIGNED;
   return cuda_status(launch_route(logits, T, E, k, topk_idx, topk_w,
@@ -123,7 +125,7 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
 
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                               int32_t has_shared, int32_t prefill) {
-  if (T < 1 || k < 1 || E < 1 || H < 1 || I < 1 || k > E) return 0;
+  if (T < 1 || k < 1 || E < 1 || H < 1 || I < 1 || k > E) return 0;   // T = 0 needs none
   if (!prefill) {
     if (T > kMaxDecodeT) return 0;
     const int sms = sm_count();   // grid of the decode kernel on the current device
@@ -146,7 +148,7 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
                               void* stream) {
   ft_status st =
       check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
-  if (st != FT_OK) return st;
+  if (st != FT_OK || T == 0) return st;
   if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
   // smallest possible workspace first (no CUDA call), then the exact one for this device
   if (workspace_bytes < DecodeLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr, 1).total)
@@ -166,7 +168,7 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
                                void* stream) {
   ft_status st =
       check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, workspace);
-  if (st != FT_OK) return st;
+  if (st != FT_OK || T == 0) return st;
   const PrefillLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr);
   if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count();

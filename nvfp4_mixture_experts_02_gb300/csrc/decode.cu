@@ -145,11 +145,13 @@ struct Plan {
   int* seg_pair0;     // first pair of each segment; [n_seg] = n_pairs
   int* seg_cp;        // cost prefix: sum over earlier segments of the cost of one step
   int* tok_pairs;     // [T][k + 1]: pairs of each token in slot order, shared last, -1 = none
-  const uint8_t** act_ptr;   // [n_act][4]: W13 codes, W13 scales, W2 codes, W2 scales
+  const uint8_t** act_ptr;   // [n_act][4]: W13 codes, W13 scales, W2 codes, W2 scales; null
+                             // when the plan is too large for the table (computed per unit)
 };
 
-// Weight base addresses of active expert i (expert e, -1 = shared).
+// Weight base addresses of active expert i (expert e, -1 = shared), when the table exists.
 __device__ __forceinline__ void set_act_ptr(const DecodeArgs& p, const Plan& P, int i, int e) {
+  if (P.act_ptr == nullptr) return;
   const size_t rb13 = (size_t)p.H / 2, rs13 = (size_t)p.H / 16;
   const size_t rb2 = (size_t)p.I / 2, rs2 = (size_t)p.I / 16;
   const size_t n13 = 2 * (size_t)p.I, n2 = (size_t)p.H;
@@ -765,7 +767,7 @@ struct PhaseStream {
   // always in flight: the unit used now was taken by the previous call, and the one taken
   // now is used by the next, so the atomic's latency is off the critical path (grabs are
   // monotonic per CTA, so a warp that stops holds no unit anyone else needs).
-  __device__ __forceinline__ void next_unit(const Plan& P) {
+  __device__ __forceinline__ void next_unit(const DecodeArgs& p, const Plan& P) {
     int u = __shfl_sync(0xffffffffu, pend, 0);
     if (lane == 0 && u < u_hi) pend = atomicAdd(disp, 1);
     if (u >= u_hi) {
@@ -787,9 +789,19 @@ struct PhaseStream {
     const size_t rb = (size_t)K / 2, rs = (size_t)K / 16;
     const size_t r0 = MODE == kW13 ? (size_t)ij : 2 * (size_t)ij;
     const size_t r1 = MODE == kW13 ? r0 + (size_t)I : r0 + 1;
-    const int o = MODE == kW13 ? 0 : 2;
-    const uint8_t* cb = P.act_ptr[4 * ia + o];
-    const uint8_t* sb = P.act_ptr[4 * ia + o + 1];
+    const uint8_t *cb, *sb;
+    if (P.act_ptr != nullptr) {   // the plan's pointer table
+      const int o = MODE == kW13 ? 0 : 2;
+      cb = P.act_ptr[4 * ia + o];
+      sb = P.act_ptr[4 * ia + o + 1];
+    } else {                      // from the expert id (-1: the shared expert)
+      const int e = P.act_expert[ia];
+      const size_t rows = MODE == kW13 ? 2 * (size_t)p.I : (size_t)p.H;
+      cb = e >= 0 ? (MODE == kW13 ? p.w13 : p.w2) + (size_t)e * rows * ((size_t)K / 2)
+                  : (MODE == kW13 ? p.sh_w13 : p.sh_w2);
+      sb = e >= 0 ? (MODE == kW13 ? p.s13 : p.s2) + (size_t)e * rows * ((size_t)K / 16)
+                  : (MODE == kW13 ? p.sh_s13 : p.sh_s2);
+    }
     ic0 = cb + r0 * rb + lane * 16;
     ic1 = cb + r1 * rb + lane * 16;
     isp = sb + ((lane >> 4) ? r1 : r0) * rs + (lane & 15) * 4;
@@ -800,7 +812,7 @@ struct PhaseStream {
   // Slot layout: row 0 codes [0, 512), row 1 codes [512, 1024), row 0 scales
   // [1024, 1088), row 1 scales [1120, 1184), header [1216, 1232): seg, j, a, ks. Lanes
   // past the end of a short row copy nothing.
-  __device__ __forceinline__ void issue_next(const Plan& P, uint32_t slot) {
+  __device__ __forceinline__ void issue_next(const DecodeArgs& p, const Plan& P, uint32_t slot) {
     if (iks < nks) {
       cp_async16(slot + lane * 16, ic0);
       cp_async16(slot + 512 + lane * 16, ic1);
@@ -811,7 +823,7 @@ struct PhaseStream {
     ic1 += 512;
     isp += 64;
     ++n_issued;
-    if (++iks == S) next_unit(P);
+    if (++iks == S) next_unit(p, P);
   }
 
   __device__ void start(const DecodeArgs& p, const Plan& P, unsigned char* ring_base,
@@ -832,10 +844,10 @@ struct PhaseStream {
     u_hi = unit_hi;
     n_issued = 0;
     pend = lane == 0 ? atomicAdd(disp, 1) : 0;
-    next_unit(P);
+    next_unit(p, P);
 #pragma unroll 1
     for (int d = 0; d < D; ++d) {
-      if (iu >= 0) issue_next(P, ring + d * kDecodeSlot);
+      if (iu >= 0) issue_next(p, P, ring + d * kDecodeSlot);
       cp_commit();   // one group per slot, empty or not: the wait count stays uniform
     }
   }
@@ -862,7 +874,7 @@ struct PhaseStream {
       const uint32_t scw = lds_u16(ls) | (lds_u16(ls + 96) << 16);
       const int4 hd = lds_i4(sa + 1216);   // seg, j, a, ks of this step
       __syncwarp();       // the slot is read before it is refilled
-      if (iu >= 0) issue_next(P, sa);
+      if (iu >= 0) issue_next(p, P, sa);
       cp_commit();
       sa += kDecodeSlot;
       if (sa == ring_end) sa = ring;
@@ -1025,7 +1037,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   P.seg_pair0 = reinterpret_cast<int*>(smem_raw + L.seg_pair0);
   P.seg_cp = reinterpret_cast<int*>(smem_raw + L.seg_cp);
   P.tok_pairs = reinterpret_cast<int*>(smem_raw + L.tok_pairs);
-  P.act_ptr = reinterpret_cast<const uint8_t**>(smem_raw + L.act_ptr);
+  P.act_ptr = L.act_ptr_table ? reinterpret_cast<const uint8_t**>(smem_raw + L.act_ptr) : nullptr;
   char* stage = reinterpret_cast<char*>(smem_raw + L.stage);
   unsigned char* ring = smem_raw + L.ring;
   const size_t stage_cap = (size_t)p.smem_bytes - L.stage;
@@ -1044,7 +1056,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   };
 
   const bool has_shared = p.sh_g13 != nullptr;
-  const bool x_on_chip = decode_x_on_chip(p.T, p.H);
+  const bool x_on_chip = L.x_on_chip;
   char* xs = x_on_chip ? reinterpret_cast<char*>(smem_raw + L.xs) : reinterpret_cast<char*>(p.xf);
   const size_t xrow = decode_act_row_bytes(p.H);
   XRegs xr;
@@ -1224,7 +1236,8 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   err = take(16);
   bar = take(16);
-  xf = take(decode_x_on_chip(T, H) ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
+  const bool x_on_chip = DecodeSmem(T, k, E, H, I, shared).x_on_chip;
+  xf = take(x_on_chip ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
   xscale = take(sizeof(float) * 2 * (size_t)T);
   h = take((size_t)max_pairs * decode_act_row_bytes(I));
   // one token: per CTA, at most ceil(W13 units / grid) or ceil(row pairs / grid) * experts
@@ -1256,15 +1269,23 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
   seg_pair0 = take(4 * (size_t)(ms + 1));
   seg_cp = take(4 * (size_t)(ms + 1));
   tok_pairs = take(4 * (size_t)T * (k + 1));
-  act_ptr = take(8 * 4 * (size_t)ma);
-  xs = take(decode_x_on_chip(T, H) ? (size_t)T * decode_act_row_bytes(H) : 0);   // x on chip
+  act_ptr_table = ma <= kDecodePtrTable;
+  act_ptr = take(act_ptr_table ? 8 * 4 * (size_t)ma : 0);
   const size_t ring_bytes = (size_t)decode_warps(T) * kDecodeDepth * kDecodeSlot;
-  ring = take(ring_bytes);   // per-warp weight-step rings
-  stage = take(0);
   // the plan's scratch (several tokens) lives in the rings and the staging area before
   // either is used
   const size_t scratch = T > 1 ? (size_t)E * 8 + 4 + (size_t)T * k * 9 + 16 : 0;
-  total = ring + (scratch > ring_bytes ? scratch : ring_bytes);
+  const size_t tail = scratch > ring_bytes ? scratch : ring_bytes;
+  // x on chip when small, and only if the plan, x and the rings fit the CTA's budget
+  // (a large plan, up to T = 64 with k = 32 over thousands of experts, sends x to the
+  // shared global copy instead)
+  const size_t xs_bytes = (size_t)T * decode_act_row_bytes(H);
+  x_on_chip = (size_t)T * (size_t)H * 2 <= kDecodeXOnChip &&
+              (o + xs_bytes + 15) / 16 * 16 + tail <= kDecodeSmem;
+  xs = take(x_on_chip ? xs_bytes : 0);
+  ring = take(ring_bytes);   // per-warp weight-step rings
+  stage = take(0);
+  total = ring + tail;
 }
 
 cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,

@@ -14,6 +14,7 @@ constexpr size_t kDecodeXOnChip = 64 * 1024;   // f16 activations kept in each C
 constexpr size_t kDecodeSmem = 224 * 1024;     // decode shared memory (one CTA per SM)
 constexpr int kDecodeDepth = 6;                // decode: weight steps in flight per warp
 constexpr int kDecodeSlot = 1232;              // one step: 2 x 512 codes, 2 x 96 scales, header
+constexpr int kDecodePtrTable = 512;           // decode: largest plan with a pointer table
 
 // Error word bits (workspace offset 0).
 constexpr int kErrBadExpert = 1;
@@ -23,9 +24,6 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Decode keeps the f16 activations in every CTA's shared memory when they are small;
 // otherwise the CTAs convert them into one shared global copy.
-__host__ __device__ inline bool decode_x_on_chip(int T, int H) {
-  return (size_t)T * (size_t)H * 2 <= kDecodeXOnChip;
-}
 
 // Decode activation rows (x and h, f16) keep every group of 32 elements in 80 bytes (64 of
 // data, 16 of padding): a warp whose 32 lanes each read their own group then touches 32
@@ -59,6 +57,8 @@ struct DecodeSmem {
          xs = 0, ring = 0,
          stage = 0,
          total = 0;   // total = minimum; the staging area grows into whatever is granted
+  bool x_on_chip = false;   // the token activations live in every CTA's shared memory
+  bool act_ptr_table = false;   // per-expert weight pointers kept (else computed per unit)
   __host__ __device__ DecodeSmem(int T, int k, int E, int H, int I, bool shared);
 };
 

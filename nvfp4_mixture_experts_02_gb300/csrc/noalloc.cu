@@ -37,8 +37,10 @@ extern "C" ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T,
                                                  float swiglu_limit, uint16_t* out,
                                                  void* stream) {
   using namespace ftmoe;
-  if (!ex || !x || !topk_idx || !topk_w || !out) return FT_ERR_INVALID_ARG;
-  if (T < 1 || k < 1 || ex->E < 1 || k > ex->E || ex->H < 1 || ex->I < 1) return FT_ERR_INVALID_ARG;
+  if (!ex) return FT_ERR_INVALID_ARG;
+  if (T < 0 || k < 1 || ex->E < 1 || k > ex->E || ex->H < 1 || ex->I < 1) return FT_ERR_INVALID_ARG;
+  if (T == 0) return FT_OK;   // empty batch: nothing to read or write
+  if (!x || !topk_idx || !topk_w || !out) return FT_ERR_INVALID_ARG;
   if (T > kMaxDecodeT || k > kMaxTopK || ex->E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FT_ERR_CUDA;

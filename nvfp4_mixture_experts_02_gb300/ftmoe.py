@@ -169,6 +169,8 @@ def workspace_bytes(T, k, E, H, I, has_shared, prefill=False) -> int:
 def new_workspace(T, k, experts: NvFP4Experts, has_shared, prefill=False, device=None,
                   stream=None) -> torch.Tensor:
     n = workspace_bytes(T, k, experts.E, experts.H, experts.I, has_shared, prefill)
+    if n == 0 and T == 0:   # an empty batch needs no workspace
+        return torch.empty(0, dtype=torch.uint8, device=device or experts.w13.device)
     if n == 0:
         raise FtError(2, "ft_moe_workspace_bytes")
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device or experts.w13.device)

@@ -76,7 +76,7 @@ def _decode(lib, ex, T=1, k=2, x=0x20000, idx=0x30000, w=0x40000, out=0x50000, w
     (dict(ex=dict(w2=0x10008)), 3),                  # misaligned weight pointer
     (dict(call=dict(k=9)), 1),                       # k > E
     (dict(call=dict(k=0)), 1),
-    (dict(call=dict(T=0)), 1),
+    (dict(call=dict(T=-1)), 1),
     (dict(call=dict(T=65)), 2),                      # decode batch limit
     (dict(call=dict(limit=0.0)), 1),
     (dict(call=dict(limit=float("nan"))), 1),
@@ -99,4 +99,20 @@ def test_route_rejects_invalid_arguments(lib):
     assert f(0x1000, 1, 8, 9, 0x1000, 0x2000, None) == 1     # k > E
     assert f(0x1000, 1, 64, 33, 0x1000, 0x2000, None) == 2   # k > 32
     assert f(0x1002, 1, 8, 2, 0x1000, 0x2000, None) == 3     # misaligned
-    assert f(0x1000, 0, 8, 2, 0x1000, 0x2000, None) == 1     # T = 0
+    assert f(0x1000, -1, 8, 2, 0x1000, 0x2000, None) == 1    # T < 0
+
+
+def test_empty_batch_is_a_no_op(lib):
+    """T = 0: FT_OK without touching any buffer (all pointers NULL), no workspace needed."""
+    f = lib.lib()
+    ex = _experts(lib)
+    assert f.ft_moe_route(0, 0, 8, 2, 0, 0, None) == 0
+    assert f.ft_moe_workspace_bytes(0, 2, 8, 256, 128, 0, 0) == 0
+    assert f.ft_moe_workspace_bytes(0, 2, 8, 256, 128, 0, 1) == 0
+    for fn in (f.ft_moe_nvfp4_decode, f.ft_moe_nvfp4_prefill):
+        assert fn(None, 0, None, None, 2, ctypes.byref(ex), None, 7.0, None, None, 0, None) == 0
+    assert f.ft_moe_nvfp4_decode_noalloc(None, 0, None, None, 2, ctypes.byref(ex), None, 7.0,
+                                         None, None) == 0
+    # the shape checks still apply to an empty batch
+    assert f.ft_moe_nvfp4_decode(None, 0, None, None, 9, ctypes.byref(ex), None, 7.0, None,
+                                 None, 0, None) == 1
