@@ -179,10 +179,17 @@ def run_ours(args, spec, rank, world, local):
     ws = ftmoe.new_workspace(spec.T, spec.k, exps[0], spec.shared, prefill=prefill)
     outs = [torch.empty((spec.T, spec.H), dtype=torch.bfloat16, device=dev) for _ in range(n_inst)]
     call = ftmoe.prefill if prefill else ftmoe.decode
+    # one-token decode: the routed call is one launch (the kernel routes the token itself),
+    # so the call and the expert kernel are the same launch
+    fused = not prefill and spec.T == 1
 
     def step(i, with_route=True):
         lay = layers[i]
         idx, w = idxs[i]
+        if fused:
+            ftmoe.decode_routed(lay.x, lay.logits, spec.k, exps[i], shs[i],
+                                limit=spec.swiglu_limit, out=outs[i], workspace=ws)
+            return
         if with_route:
             ftmoe.route(lay.logits, spec.k, idx, w)
         call(lay.x, idx, w, exps[i], shs[i], limit=spec.swiglu_limit, out=outs[i], workspace=ws)
@@ -258,7 +265,10 @@ def run_ours(args, spec, rank, world, local):
         achieved = bytes_call / (dec_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
-                "kernel": "k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in one launch)",
+                "kernel": ("k_decode (ft_moe_nvfp4_decode_routed: routing, plan, W13+SwiGLU, "
+                           "W2+weighted sum in one launch)" if fused else
+                           "k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in "
+                           "one launch)"),
                 "us_per_launch": round(dec_us, 3)}
     res = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
@@ -276,7 +286,8 @@ def run_ours(args, spec, rank, world, local):
                    "graph": "CUDA graph of one pass over the instances",
                    "bytes_per_call": round(bytes_call), "experts_touched_mean":
                    statistics.mean(touched)},
-        "roofline": roof, "e2e": e2e, "gpu_launches": (6 if prefill else 2) * steps_done,
+        "roofline": roof, "e2e": e2e,
+        "gpu_launches": (6 if prefill else 1 if fused else 2) * steps_done,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -308,22 +319,34 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     import torch
     from nvfp4_mixture_experts_02_gb300 import ftmoe
     n = min(len(layers), 48)
-    hx = [torch.from_numpy(l.x_bits.view(np.int16)).pin_memory() for l in layers[:n]]
-    hl = [torch.from_numpy(l.logits_np).pin_memory() for l in layers[:n]]
+    # one pinned staging buffer per step input: x (bf16 bits) then the logits (fp32), so
+    # each step makes one host-to-device copy (x's bytes are a multiple of 256: the logits
+    # stay aligned)
+    nx, nl = spec.T * spec.H * 2, spec.T * spec.E * 4
+    hin = []
+    for l in layers[:n]:
+        buf = np.empty(nx + nl, np.uint8)
+        buf[:nx] = l.x_bits.view(np.uint8).reshape(-1)
+        buf[nx:] = l.logits_np.view(np.uint8).reshape(-1)
+        hin.append(torch.from_numpy(buf).pin_memory())
     hout = torch.empty((spec.T, spec.H), dtype=torch.int16).pin_memory()
-    dx = torch.empty((spec.T, spec.H), dtype=torch.int16, device=dev)
-    dl = torch.empty((spec.T, spec.E), dtype=torch.float32, device=dev)
+    din = torch.empty(nx + nl, dtype=torch.uint8, device=dev)
+    dx = din[:nx].view(torch.int16).view(spec.T, spec.H)
+    dl = din[nx:].view(torch.float32).view(spec.T, spec.E)
     out = torch.empty((spec.T, spec.H), dtype=torch.bfloat16, device=dev)
     idx = torch.empty((spec.T, spec.k), dtype=torch.int32, device=dev)
     w = torch.empty((spec.T, spec.k), dtype=torch.float32, device=dev)
     call = ftmoe.prefill if spec.prefill else ftmoe.decode
 
     def one(i):
-        dx.copy_(hx[i], non_blocking=True)
-        dl.copy_(hl[i], non_blocking=True)
-        ftmoe.route(dl, spec.k, idx, w)
-        call(dx.view(torch.bfloat16), idx, w, exps[i], shs[i], limit=spec.swiglu_limit, out=out,
-             workspace=ws)
+        din.copy_(hin[i], non_blocking=True)
+        if spec.prefill:
+            ftmoe.route(dl, spec.k, idx, w)
+            call(dx.view(torch.bfloat16), idx, w, exps[i], shs[i], limit=spec.swiglu_limit,
+                 out=out, workspace=ws)
+        else:   # the routed decode call (one launch for one token)
+            ftmoe.decode_routed(dx.view(torch.bfloat16), dl, spec.k, exps[i], shs[i],
+                                limit=spec.swiglu_limit, out=out, workspace=ws)
         hout.copy_(out.view(torch.int16), non_blocking=True)
 
     for i in range(min(n, 3)):

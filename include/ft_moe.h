@@ -136,6 +136,25 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
                               void* stream);
 
 /*
+ * ft_moe_nvfp4_decode_routed — route and decode in one call: the layer from the router
+ * logits instead of the routing slots (the softmax -> top-k -> renormalise of
+ * ft_moe_route, then ft_moe_nvfp4_decode). For T = 1 it is a single kernel launch in which
+ * every CTA routes the token itself; for T >= 2 it enqueues the route kernel and then the
+ * decode kernel. The experts, weights and output are bit-identical to ft_moe_route followed
+ * by ft_moe_nvfp4_decode.
+ *   logits        float [T, E] (4-byte aligned), must be finite
+ *   topk_idx_out  int32 [T, k] or NULL; topk_w_out float [T, k] or NULL: when given, the
+ *                 routing slots are written there (as ft_moe_route writes them)
+ *   workspace     as for ft_moe_nvfp4_decode (ft_moe_workspace_bytes(T,k,E,H,I,sh!=0,0))
+ *   other arguments, limits, T = 0 and errors: as ft_moe_nvfp4_decode.
+ */
+ft_status ft_moe_nvfp4_decode_routed(const uint16_t* x, int32_t T, const float* logits,
+                                     int32_t k, const ft_nvfp4_experts* ex,
+                                     const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                                     uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * ft_moe_nvfp4_prefill — the same layer for a multi-token chunk (any T >= 0), run as
  * grouped dense contractions: tokens are grouped by expert on the GPU, NVFP4 tiles are
  * dequantised to bf16 on chip and multiplied on the tensor cores. Arguments as for

@@ -161,6 +161,41 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
                                    out, workspace, sms, static_cast<cudaStream_t>(stream)));
 }
 
+ft_status ft_moe_nvfp4_decode_routed(const uint16_t* x, int32_t T, const float* logits,
+                                     int32_t k, const ft_nvfp4_experts* ex,
+                                     const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                                     uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  ft_status st = check_experts(ex, sh);
+  if (st != FT_OK) return st;
+  if (T < 0 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!(swiglu_limit > 0.0f) || !(swiglu_limit <= 128.0f)) return FT_ERR_INVALID_ARG;
+  if (T == 0) return FT_OK;
+  if (!x || !logits || !out || !workspace) return FT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) || !aligned(workspace, 256) ||
+      !aligned(topk_idx_out, 4) || !aligned(topk_w_out, 4))
+    return FT_ERR_MISALIGNED;
+  if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < DecodeLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr, 1).total)
+    return FT_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return FT_ERR_CUDA;
+  const DecodeLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr, sms < kMaxGrid ? sms : kMaxGrid);
+  if (workspace_bytes < L.total) return FT_ERR_WORKSPACE_TOO_SMALL;
+  const ExpertPtrs ptrs = to_ptrs(ex, sh);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 1)   // one launch: every CTA routes the token itself
+    return cuda_status(launch_decode(x, 1, nullptr, nullptr, k, ptrs, swiglu_limit, out,
+                                     workspace, sms, s, logits, topk_idx_out, topk_w_out));
+  char* base = static_cast<char*>(workspace);
+  int* idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int*>(base + L.topk);
+  float* w = topk_w_out ? topk_w_out : reinterpret_cast<float*>(base + L.topk + 4 * (size_t)T * k);
+  cudaError_t e = launch_route(logits, T, ex->E, k, idx, w, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_decode(x, T, idx, w, k, ptrs, swiglu_limit, out, workspace, sms, s));
+}
+
 ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk_idx,
                                const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
                                const ft_nvfp4_shared_expert* sh, float swiglu_limit,

@@ -37,6 +37,7 @@
 
 #include "ftmoe_device.cuh"
 #include "ftmoe_internal.h"
+#include "ftmoe_route.cuh"
 
 namespace ftmoe {
 
@@ -62,6 +63,9 @@ struct DecodeArgs {
   int T, k, E, H, I;
   const int* topk_idx;
   const float* topk_w;
+  const float* logits;   // one token, routed in the kernel: [E] (then topk_* are outputs or null)
+  int* topk_idx_out;     // routed in the kernel: where CTA 0 writes the k slots (or null)
+  float* topk_w_out;
   const uint8_t *w13, *s13, *w2, *s2;
   const float *g13, *g2;
   const uint8_t *sh_w13, *sh_s13, *sh_w2, *sh_s2;
@@ -366,14 +370,15 @@ struct PlanT1Regs {
 // is all the weight stream needs to start. The tensor scales are loaded here but first
 // used by finish_plan_t1, after the stream has started, so their latency is off the path
 // to the first weight copy.
-__device__ PlanT1Regs build_plan_t1(const DecodeArgs& p, const Plan& P) {
+// e_in / w_in: warp 0's routing slots (lane r < k holds slot r).
+__device__ PlanT1Regs build_plan_t1(const DecodeArgs& p, const Plan& P, int e_in, float w_in) {
   const int tid = threadIdx.x, lane = tid & 31;
   const bool has_shared = p.sh_g13 != nullptr;
   PlanT1Regs r{0.f, 0.f, 0.f, 0.f, 0.f, 0, 0, false};
   if (tid < 32) {
     const int k = p.k;
-    const int e = lane < k ? p.topk_idx[lane] : -1;
-    r.w = lane < k ? p.topk_w[lane] : 0.f;
+    const int e = lane < k ? e_in : -1;
+    r.w = lane < k ? w_in : 0.f;
     bool ok = lane < k && e >= 0 && e < p.E;
     for (int j = 0; j < k; ++j) {   // an id repeated in earlier slots is dropped
       const int ej = __shfl_sync(0xffffffffu, e, j);
@@ -507,33 +512,33 @@ __device__ void convert_token(const DecodeArgs& p, int t, char* dst, float* s_sc
 
 // Single token: this thread's 16-byte chunks of x and of the shared-expert gate, loaded
 // into registers before the weight stream starts so that they are not queued behind it.
-constexpr int kXChunks = 4;   // H <= 16384 elements over 512 threads
-struct XRegs {
-  uint4 x[kXChunks], g[kXChunks];
-};
-
-__device__ void x_t1_load(const DecodeArgs& p, XRegs& r) {
-#pragma unroll
-  for (int c = 0; c < kXChunks; ++c) {
-    const int e = (threadIdx.x + c * blockDim.x) * 8;
-    r.x[c] = r.g[c] = make_uint4(0, 0, 0, 0);
-    if (e < p.H) {
-      r.x[c] = *reinterpret_cast<const uint4*>(p.x + e);
-      if (p.sh_gate) r.g[c] = *reinterpret_cast<const uint4*>(p.sh_gate + e);
-    }
-  }
+// One token: warps 1..15 (kConvThreads threads, named barrier 1) load x and the shared
+// gate vector, reduce max|x| and the gate dot product, and write x' = x / 2^s (max|x'| in
+// [256, 512)) as a padded f16 row, while warp 0 obtains the routing slots.
+constexpr int kConvThreads = 480;
+constexpr int kConvChunks = 5;   // 16-byte pieces per thread: H <= 16384 = 2048 pieces
+__device__ __forceinline__ void conv_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory");
 }
 
-// The same conversion as convert_token, from the registers.
-__device__ void x_t1_convert(const DecodeArgs& p, const XRegs& r, char* dst, float* s_scale,
-                             float* s_dot) {
-  __shared__ float red_a[32], red_d[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+__device__ void x_t1_convert(const DecodeArgs& p, char* dst, float* s_scale, float* s_dot) {
+  __shared__ float red_a[kConvThreads / 32], red_d[kConvThreads / 32];
+  const int t = threadIdx.x - 32, lane = t & 31, warp = t >> 5;
+  uint4 xv[kConvChunks], gv[kConvChunks];
+#pragma unroll
+  for (int c = 0; c < kConvChunks; ++c) {
+    const int e = (t + c * kConvThreads) * 8;
+    xv[c] = gv[c] = make_uint4(0, 0, 0, 0);
+    if (e < p.H) {
+      xv[c] = *reinterpret_cast<const uint4*>(p.x + e);
+      if (p.sh_gate) gv[c] = *reinterpret_cast<const uint4*>(p.sh_gate + e);
+    }
+  }
   float amax = 0.f, dot = 0.f;
 #pragma unroll
-  for (int c = 0; c < kXChunks; ++c) {
-    const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
-    const uint32_t gw[4] = {r.g[c].x, r.g[c].y, r.g[c].z, r.g[c].w};
+  for (int c = 0; c < kConvChunks; ++c) {
+    const uint32_t w[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+    const uint32_t gw[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
@@ -551,10 +556,10 @@ __device__ void x_t1_convert(const DecodeArgs& p, const XRegs& r, char* dst, flo
     red_a[warp] = amax;
     red_d[warp] = dot;
   }
-  __syncthreads();
-  if (tid == 0) {
+  conv_barrier();
+  if (t == 0) {
     float a = 0.f, d = 0.f;
-    for (int w = 0; w < nw; ++w) {   // fixed order: reproducible
+    for (int w = 0; w < kConvThreads / 32; ++w) {   // fixed order: reproducible
       a = fmaxf(a, red_a[w]);
       d += red_d[w];
     }
@@ -566,13 +571,13 @@ __device__ void x_t1_convert(const DecodeArgs& p, const XRegs& r, char* dst, flo
     *s_scale = ldexpf(1.f, ex);
     *s_dot = d;
   }
-  __syncthreads();
+  conv_barrier();
   const float down = 1.f / *s_scale;
 #pragma unroll
-  for (int c = 0; c < kXChunks; ++c) {
-    const int e = (tid + c * blockDim.x) * 8;
+  for (int c = 0; c < kConvChunks; ++c) {
+    const int e = (t + c * kConvThreads) * 8;
     if (e < p.H) {
-      const uint32_t w[4] = {r.x[c].x, r.x[c].y, r.x[c].z, r.x[c].w};
+      const uint32_t w[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -583,7 +588,6 @@ __device__ void x_t1_convert(const DecodeArgs& p, const XRegs& r, char* dst, flo
       *reinterpret_cast<uint4*>(dst + act_byte(e)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
-  __syncthreads();
 }
 
 // -------------------------------------------------------------------- the GEMV phases
@@ -1059,11 +1063,31 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   const bool x_on_chip = L.x_on_chip;
   char* xs = x_on_chip ? reinterpret_cast<char*>(smem_raw + L.xs) : reinterpret_cast<char*>(p.xf);
   const size_t xrow = decode_act_row_bytes(p.H);
-  XRegs xr;
-  if (NT == 1) x_t1_load(p, xr);   // before the weight stream
-
   PlanT1Regs t1r{};
-  if (NT == 1) t1r = build_plan_t1(p, P);
+  if (NT == 1) {
+    // the token's routing slots, by warp 0: given, or routed here from its logits in every
+    // CTA (the same warp routine as the route kernel: the same experts and weights), while
+    // warps 1..15 convert x into shared memory
+    int e_in = -1;
+    float w_in = 0.f;
+    if (tid >= 32) {
+      x_t1_convert(p, xs, &s_scale, &s_dot);
+    } else {
+      const int lane = tid & 31;
+      if (p.logits != nullptr) {
+        route_warp_any(p.logits, p.E, p.k, lane, e_in, w_in);
+        if (blockIdx.x == 0 && lane < p.k) {
+          if (p.topk_idx_out) p.topk_idx_out[lane] = e_in;
+          if (p.topk_w_out) p.topk_w_out[lane] = w_in;
+        }
+      } else if (lane < p.k) {
+        e_in = p.topk_idx[lane];
+        w_in = p.topk_w[lane];
+      }
+    }
+    __syncthreads();   // x' and its scale are in shared memory
+    t1r = build_plan_t1(p, P, e_in, w_in);
+  }
   else build_plan<NT>(p, P, reinterpret_cast<int*>(ring));
   if (tid == 0) {
     cta_units<NT, kW13>(p, P, s_range[0], s_range[1]);
@@ -1081,8 +1105,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
 
   // activations: every CTA converts all tokens into its shared memory (small T), or the
   // CTAs convert one token each into a shared global copy (larger T), then a grid barrier
-  if (NT == 1) {
-    x_t1_convert(p, xr, xs, &s_scale, &s_dot);
+  if (NT == 1) {   // x converted before the plan; thread 0 wrote misc[4] in finish_plan_t1
     if (tid == 0) {
       P.xscale[0] = s_scale;
       if (has_shared)
@@ -1246,6 +1269,7 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   upart_units = (int)(u13 > u2 ? u13 : u2);
   upart = take(T == 1 ? sizeof(float2) * 8 * (size_t)grid * upart_units : 16);
   part = take(T > 1 ? sizeof(float) * (size_t)max_pairs * H : 16);
+  topk = take(8 * (size_t)T * k);
   total = o;
 }
 
@@ -1290,7 +1314,8 @@ __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bo
 
 cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
                           int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
-                          int num_sms, cudaStream_t stream) {
+                          int num_sms, cudaStream_t stream, const float* logits,
+                          int* topk_idx_out, float* topk_w_out) {
   const bool shared = ex.sh_w13 != nullptr;
   const int grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
   const DecodeLayout WL(T, k, ex.E, ex.H, ex.I, shared, grid);
@@ -1305,6 +1330,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   DecodeArgs a;
   a.x = x; a.T = T; a.k = k; a.E = ex.E; a.H = ex.H; a.I = ex.I;
   a.topk_idx = topk_idx; a.topk_w = topk_w;
+  a.logits = logits; a.topk_idx_out = topk_idx_out; a.topk_w_out = topk_w_out;
   a.w13 = ex.w13; a.s13 = ex.s13; a.w2 = ex.w2; a.s2 = ex.s2; a.g13 = ex.g13; a.g2 = ex.g2;
   a.sh_w13 = shared ? ex.sh_w13 : nullptr; a.sh_s13 = shared ? ex.sh_s13 : nullptr;
   a.sh_w2 = shared ? ex.sh_w2 : nullptr; a.sh_s2 = shared ? ex.sh_s2 : nullptr;

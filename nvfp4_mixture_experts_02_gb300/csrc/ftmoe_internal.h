@@ -23,9 +23,12 @@ struct ExpertPtrs {
   const uint16_t* sh_gate;
 };
 
+// logits != null (T = 1 only): the kernel routes the token itself (topk_idx / topk_w are
+// then ignored) and CTA 0 writes the slots to topk_idx_out / topk_w_out when not null.
 cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
                           int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
-                          int num_sms, cudaStream_t stream);
+                          int num_sms, cudaStream_t stream, const float* logits = nullptr,
+                          int* topk_idx_out = nullptr, float* topk_w_out = nullptr);
 
 // Workspace regions of the prefill path (byte offsets, 256-byte aligned).
 struct PrefillLayout {

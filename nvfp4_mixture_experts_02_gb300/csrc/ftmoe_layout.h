@@ -45,7 +45,9 @@ struct DecodeLayout {
   int max_act = 0;     // active experts (routed, distinct) + shared
   int max_pairs = 0;   // (token, expert) pairs incl. the shared expert's T pairs
   int upart_units = 0;   // units per CTA slice of the one-token partial sums
-  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, upart = 0, part = 0, total = 0;
+  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, upart = 0, part = 0,
+         topk = 0,   // routed decode of several tokens: the routing slots [T][k] idx, then w
+         total = 0;
   DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid);
 };
 

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_UNSUPPORTED_SHAP
 
 EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_workspace_bytes",
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
-            "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc"]
+            "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
+            "ft_moe_nvfp4_decode_routed"]
 
 
 class FtError(RuntimeError):
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         getattr(lib, name).argtypes = layer
     lib.ft_moe_nvfp4_decode_noalloc.restype = ctypes.c_int
     lib.ft_moe_nvfp4_decode_noalloc.argtypes = layer[:9] + [vp]
+    lib.ft_moe_nvfp4_decode_routed.restype = ctypes.c_int
+    lib.ft_moe_nvfp4_decode_routed.argtypes = [vp, i32, vp, i32, ctypes.POINTER(_Experts),
+                                               ctypes.POINTER(_Shared), f32, vp, vp, vp, vp, sz,
+                                               vp]
     lib.ft_moe_last_cuda_error.restype = ctypes.c_char_p
     lib.ft_moe_get_error.restype = ctypes.c_int
     lib.ft_moe_get_error.argtypes = [vp, vp]
@@ -218,6 +223,25 @@ def decode_noalloc(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=Non
                                           ctypes.byref(sh) if sh is not None else None,
                                           float(limit), _ptr(out), _stream(stream))
     _check(st, "ft_moe_nvfp4_decode_noalloc")
+    return out
+
+
+def decode_routed(x, logits, k, experts, shared=None, limit=7.0, out=None, topk_idx=None,
+                  topk_w=None, workspace=None, stream=None):
+    """ft_moe_nvfp4_decode_routed: the layer from the router logits f32 [T,E] (T <= 64); one
+    launch for T = 1. topk_idx / topk_w (int32 / f32 [T,k]), when given, receive the slots."""
+    T = x.shape[0]
+    if workspace is None:
+        workspace = new_workspace(T, k, experts, shared is not None, stream=stream)
+    if out is None:
+        out = torch.empty((T, experts.H), dtype=torch.bfloat16, device=x.device)
+    ex = experts.cstruct()
+    sh = shared.cstruct() if shared is not None else None
+    st = _LIB.ft_moe_nvfp4_decode_routed(_ptr(x), T, _ptr(logits), k, ctypes.byref(ex),
+                                         ctypes.byref(sh) if sh is not None else None,
+                                         float(limit), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+                                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "ft_moe_nvfp4_decode_routed")
     return out
 
 
