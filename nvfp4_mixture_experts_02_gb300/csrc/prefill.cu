@@ -29,6 +29,8 @@
 // the MMAs.
 #include <cmath>
 #include <cstdint>
+#include <cuda.h>          // CUtensorMap (the encoder is fetched through the runtime)
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "ftmoe_internal.h"
@@ -47,6 +49,12 @@ constexpr int kPfBStages = 8;             // activation tiles in shared memory (
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 stages x 2 x 32 cols
 constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 16 KB per stage
+// weight codes: a tile is 4 chunks (128 bytes) of the item's 256 rows, two tensor-map copies
+// (one per 128-row set, 128-byte swizzle) into one of kPfWTiles slots
+constexpr int kPfTileChunks = 4;
+constexpr int kWSetBytes = 128 * 128;
+constexpr int kWTileBytes = 2 * kWSetBytes;                        // 32 KB
+constexpr int kPfWTiles = 3;
 
 struct PfPlanArgs {
   const int* topk_idx;
@@ -289,6 +297,8 @@ struct PfGemmArgs {
   float* part_out;        // W2 output (fp32 per pair)
   float limit, oscale_mul;  // W2: output scale = g2ref * oscale_mul (= 1 / 2^S)
   int* err;
+  // the codes as 2D uint8 tensors [rows][K/2] (routed: all experts' rows; shared expert)
+  CUtensorMap tm_w, tm_sh_w;
 };
 
 // 16-byte cp.async to shared memory; src_bytes < 16 zero-fills the rest (0: no read).
@@ -299,20 +309,29 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, 
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
+// One box of a 2D tensor map into shared memory, completing on `bar` (x: byte offset in
+// the row, a multiple of 16; y: row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// 16 bytes of a weight row. L1-allocating: a thread reads its row 32 bytes per chunk, so
-// one 128-byte line serves four chunks from L1 (no-allocate loads or an evict-first L2
-// policy measured 9% slower on the whole layer).
-__device__ __forceinline__ uint4 ldg_weights16(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
 }
 
 template <bool kW13>
@@ -320,6 +339,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   extern __shared__ __align__(1024) unsigned char pf_smem[];
   __shared__ __align__(8) uint64_t mbar_full[kPfStages];
   __shared__ __align__(8) uint64_t mbar_done[kPfStages];
+  __shared__ __align__(8) uint64_t mbar_w[kPfWTiles];   // code tile landed
   __shared__ uint32_t tmem_base_slot;
   __shared__ int s_tok[kPfN];
   __shared__ float s_w[kPfN];
@@ -330,6 +350,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   const int set = (warp >> 2) & 1;           // row set 0 / 1 (producers)
   const int m = (warp & 3) * 32 + lane;      // row inside the set = TMEM lane
   unsigned char* sB = pf_smem;               // [kPfBStages][kBTileBytes]
+  const uint32_t sW = smem_addr(pf_smem + kPfBStages * kBTileBytes);   // [kPfWTiles][2 sets][128][128 B]
   (void)lane;
 
   if (warp == 0) {
@@ -344,6 +365,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       mbar_init(&mbar_full[s], kPfProducers);
       mbar_init(&mbar_done[s], 1);
     }
+    for (int s = 0; s < kPfWTiles; ++s) mbar_init(&mbar_w[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -365,6 +387,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   // completed n / kPfStages phases (the parities follow from n, no per-stage counters:
   // a dynamically indexed array would live in local memory and slow the MMA issue)
   uint32_t nprod = 0;
+  uint32_t ntile = 0;   // code tiles of the earlier items: tile g uses slot g % kPfWTiles
   bool ok = true;
 
   for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -382,6 +405,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     const size_t nrows = kW13 ? 2 * (size_t)p.I : (size_t)p.H;
     const uint8_t* wrow = (e >= 0 ? p.w + (size_t)e * nrows * rowb : p.sh_w) + (size_t)row * rowb;
     const uint8_t* srow = (e >= 0 ? p.s + (size_t)e * nrows * srowb : p.sh_s) + (size_t)row * srowb;
+    // code tiles of this item: rows of set 0 / set 1 in the tensor map, one tile per 4 chunks
+    const int ntiles = (nchunks + kPfTileChunks - 1) / kPfTileChunks;
+    const CUtensorMap* tmap = e >= 0 ? &p.tm_w : &p.tm_sh_w;
+    const int ybase = e >= 0 ? e * (int)nrows : 0;
+    const int y0 = ybase + (kW13 ? rb * 128 : rb * 256);
+    const int y1 = ybase + (kW13 ? p.I + rb * 128 : rb * 256 + 128);
+    auto issue_tile = [&](int t) {   // one elected thread
+      const uint32_t g = ntile + (uint32_t)t;
+      const int slot = (int)(g % kPfWTiles);
+      const uint32_t dst = sW + (uint32_t)(slot * kWTileBytes);
+      mbar_arrive_tx(&mbar_w[slot], kWTileBytes);
+      tma_load_2d(dst, tmap, t * 128, y0, &mbar_w[slot]);
+      tma_load_2d(dst + kWSetBytes, tmap, t * 128, y1, &mbar_w[slot]);
+    };
     if (tid < kPfN) {
       const int n = tid;
       s_tok[n] = n < nv ? p.pair_tok[p0 + n] : 0;
@@ -392,18 +429,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     }
     __syncthreads();
 
-    // register pipeline of the weight stream: codes and scales, kPfStages deep
-    uint4 q[kPfStages][2];
+    // register pipeline of the scales (4 bytes a chunk, L1-allocating), kPfStages deep;
+    // the codes come as tiles through the tensor-memory-access engine (issue_tile)
+    (void)wrow;
     uint32_t sc[kPfStages];
     auto issue = [&](int d, int c) {
-      if (row_ok) {
-        q[d][0] = ldg_weights16(wrow + (size_t)c * 32);
-        q[d][1] = ldg_weights16(wrow + (size_t)c * 32 + 16);
-        sc[d] = __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)c * 4));
-      } else {
-        q[d][0] = q[d][1] = make_uint4(0, 0, 0, 0);
-        sc[d] = 0;
-      }
+      sc[d] = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)c * 4)) : 0u;
     };
     // the group's activation tile of chunk c straight into shared-memory stage bst
     // (cp.async, no registers; padding rows n >= nv are zero-filled): one commit group
@@ -424,12 +455,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     };
     const uint32_t idesc = idesc_f16(128, npad);
     if (!producer) {
-      // ---- MMA warp: for each chunk, wait until every producer has filled the stage,
-      // issue its MMAs (lane 0) and commit them to the stage's "done" barrier
+      // ---- MMA warp: sends the item's code tiles (the first three now; tile t + 3 once
+      // every producer is past tile t, i.e. the "full" barrier of its last chunk has
+      // completed), and for each chunk waits until every producer has filled the stage,
+      // issues its MMAs and commits them to the stage's "done" barrier
+      if (lane == 0)
+        for (int t = 0; t < kPfWTiles && t < ntiles; ++t) issue_tile(t);
+      __syncwarp();
       for (int c = 0; c < nchunks && ok; ++c) {
         const int st = (int)(nprod % kPfStages);
         ok = mbar_wait(&mbar_full[st], (nprod / kPfStages) & 1, p.err, kErrTimeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
+        const int t = c / kPfTileChunks;
+        if (lane == 0 && ok && (c % kPfTileChunks == kPfTileChunks - 1 || c == nchunks - 1) &&
+            t + kPfWTiles < ntiles)
+          issue_tile(t + kPfWTiles);
+        __syncwarp();
         tc_fence_after();
         {   // the whole warp passes the operands, one elected lane issues
           const uint32_t b0 = smem_addr(sB + (int)(nprod % kPfBStages) * kBTileBytes);
@@ -462,6 +503,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       }
     }
     for (int c0 = 0; c0 < nchunks && ok; c0 += kPfStages) {
+      // this thread's row of code tile c0 / 4 (chunks c0..c0+3): 16-byte pieces 2d and
+      // 2d + 1 of its 128-byte row, stored at piece ^ (row % 8) by the 128-byte swizzle
+      const uint32_t g = ntile + (uint32_t)(c0 / kPfTileChunks);
+      ok = ok && mbar_wait(&mbar_w[g % kPfWTiles], (g / kPfWTiles) & 1, p.err, kErrTimeout);
+      const uint32_t rbase = sW + (uint32_t)((g % kPfWTiles) * kWTileBytes + set * kWSetBytes + m * 128);
+      const uint32_t sw = (uint32_t)(m & 7);
 #pragma unroll
       for (int d = 0; d < kPfStages; ++d) {
         const int c = c0 + d;
@@ -473,7 +520,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           if (c + kPfStages < nchunks) issue_b(c + kPfStages, (int)((nprod + kPfStages) % kPfBStages));
           else cp_async_commit();
           uint32_t r[32];
-          dequant64(q[d][0], q[d][1], sc[d], r);
+          dequant64(lds_v4(rbase + (((2 * d) ^ sw) << 4)), lds_v4(rbase + (((2 * d + 1) ^ sw) << 4)),
+                    sc[d], r);
           tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
           if (c + kPfStages < nchunks) issue(d, c + kPfStages);
           cp_async_wait<kPfStages>();   // this chunk's activation tile has landed
@@ -531,6 +579,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     }
     tc_fence_before();
     __syncthreads();   // accumulators read before the next item's first MMA
+    ntile += (uint32_t)ntiles;
   }
 
   tc_fence_before();
@@ -616,6 +665,29 @@ PrefillLayout::PrefillLayout(int T, int k, int E, int H, int I, bool shared) {
   total = o;
 }
 
+// 2D uint8 tensor map over `rows` rows of `row_bytes` bytes: boxes of 128 bytes x 128 rows,
+// 128-byte swizzle, zero fill past the tensor (rows past an expert read the next expert's,
+// which only ever land in rows whose results are dropped).
+bool code_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
                            int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
                            int num_sms, cudaStream_t stream) {
@@ -651,7 +723,7 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
     cudaLaunchConfig_t cfg = pdl_cfg(dim3((T + 7) / 8), dim3(256), 0, stream, at);
     if ((err = cudaLaunchKernelEx(&cfg, k_pf_act, aa)) != cudaSuccess) return err;
   }
-  const size_t smem = (size_t)kPfBStages * kBTileBytes;
+  const size_t smem = (size_t)kPfBStages * kBTileBytes + (size_t)kPfWTiles * kWTileBytes;
   static bool attr_set[64] = {};
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -677,6 +749,10 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   g.b_src = reinterpret_cast<const __half*>(base + L.xf); g.xscale = F32(L.xscale);
   g.h_out = reinterpret_cast<__half*>(base + L.h); g.part_out = nullptr; g.limit = limit;
   g.oscale_mul = 1.0f / hscale; g.err = I32(L.err);
+  // code tensor maps: W13 [E*2I][H/2], W2 [E*H][I/2] (and the shared expert's)
+  if (!code_map(&g.tm_w, ex.w13, (uint64_t)ex.H / 2, (uint64_t)ex.E * 2 * ex.I)) return cudaErrorInvalidValue;
+  if (shared && !code_map(&g.tm_sh_w, ex.sh_w13, (uint64_t)ex.H / 2, 2 * (uint64_t)ex.I))
+    return cudaErrorInvalidValue;
   {
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_cfg(dim3(num_sms), dim3(kPfThreads), smem_launch, stream, at);
@@ -686,6 +762,9 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   g2.w = ex.w2; g2.s = ex.s2; g2.sh_w = ex.sh_w2; g2.sh_s = ex.sh_s2;
   g2.b_src = reinterpret_cast<const __half*>(base + L.h); g2.h_out = nullptr;
   g2.part_out = reinterpret_cast<float*>(base + L.part);
+  if (!code_map(&g2.tm_w, ex.w2, (uint64_t)ex.I / 2, (uint64_t)ex.E * ex.H)) return cudaErrorInvalidValue;
+  if (shared && !code_map(&g2.tm_sh_w, ex.sh_w2, (uint64_t)ex.I / 2, (uint64_t)ex.H))
+    return cudaErrorInvalidValue;
   {
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_cfg(dim3(num_sms), dim3(kPfThreads), smem_launch, stream, at);
