@@ -15,11 +15,14 @@
 // item is one token group of one expert (up to 128 tokens, the MMA N) against 256 weight
 // rows: for W13 the 128 gate rows and the 128 matching up rows of a row block (two fp32
 // accumulators in tensor memory, so SwiGLU pairs land in the same TMEM lane), for W2 two
-// 128-row blocks of the output. Each producer thread owns one weight row: it streams the
-// row's packed E2M1 codes and E4M3 scales with 16-byte L1-allocating loads (a register
-// pipeline 4 chunks deep), forms e2m1*e4m3 exactly in f16 (hardware conversions + one
-// f16x2 multiply per pair) and writes it into tensor memory (tcgen05.st) as the MMA's A
-// operand. The group's activations (B operand) go straight from global to shared memory
+// 128-row blocks of the output. The item's weight codes arrive as tiles of 4 chunks (256
+// rows x 128 bytes) through the tensor-memory-access engine (two 2D tensor-map copies per
+// tile, 128-byte swizzle, three tile slots), sent by the MMA warp once every producer is
+// past the tile the slot held. Each producer thread owns one weight row: it reads its
+// row's 32 code bytes of a chunk from the tile, takes the E4M3 scales through a small
+// register pipeline (L1-allocating loads), forms e2m1*e4m3 exactly in f16 (hardware
+// conversions + one f16x2 multiply per pair) and writes it into tensor memory
+// (tcgen05.st) as the MMA's A operand. The group's activations (B operand) go straight from global to shared memory
 // by cp.async, in the canonical K-major core-matrix layout, 4 chunks ahead in 8 stages.
 // Every producer arrives on the stage's "full" mbarrier when its part of a chunk is in
 // place; the MMA warp waits for the stage and, as a whole converged warp with one elected
