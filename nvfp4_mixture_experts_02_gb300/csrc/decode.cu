@@ -1,7 +1,8 @@
 // Decode path of the NVFP4 MoE layer (1 <= T <= 64) as ONE persistent cooperative kernel:
 //
-//   plan (every CTA, shared memory) -> f16 activations -> W13 + clamped SwiGLU
-//   -> grid barrier -> W2 + router-weighted top-k sum [-> grid barrier -> per-token sum]
+//   [routing of the token (one token, routed call)] -> plan (every CTA, shared memory)
+//   -> f16 activations -> W13 + clamped SwiGLU -> grid barrier -> W2 + router-weighted
+//   top-k sum [-> grid barrier -> per-token sum]
 //
 // At decode sizes every (token, expert) pair sees a handful of tokens, so the work is a
 // batch of matrix-vector products bound by the weight stream; it runs on the CUDA cores as
@@ -20,14 +21,17 @@
 //
 // Work split. W13 unit = gate row j and up row j of one segment (a run of at most NT of
 // one expert's pairs), so the SwiGLU pair of every output lands in one warp. W2 unit = a
-// pair of output rows: for one token (NT == 1) its reduction runs over (active expert, i)
-// with the router weights already folded into h, so one sum yields the weighted top-k sum
-// plus the shared expert; for several tokens it runs over one segment's pairs and the
-// per-pair results are summed per token after a last grid barrier. The (unit, step) list
-// of a phase is cut into equal contiguous ranges, one per warp of the grid, so every warp
-// streams the same number of weight bytes; a unit cut by a range boundary is finished by
-// the last warp to arrive (a counter per split unit), which adds the partial sums in warp
-// order. The output bits are reproducible for a given device.
+// pair of output rows: for one token (NT == 1) of one active expert, with the router
+// weights already folded into h, so the sum over the units of a row pair is the weighted
+// top-k sum plus the shared expert; for several tokens over one segment's pairs, the
+// per-pair results summed per token after a last grid barrier. Every CTA gets a contiguous
+// range of whole units of equal cost (cost of a step: kCostBase + kCostTok * tokens), and
+// its warps take units from a shared-memory counter, so faster warps take more and no
+// unit is split. Each warp streams its steps through a private ring of shared-memory
+// slots filled by cp.async ahead of the compute. One token: a unit's lane sums are folded
+// to 8 partials and the CTA finishes its units after the phase in a fixed order; several
+// tokens: warp reduction and finish per unit. The output bits are reproducible for a
+// given device.
 //
 // Every device-side wait is bounded and reports FT_ERR_TIMEOUT instead of hanging.
 #include <cfloat>
@@ -510,8 +514,6 @@ __device__ void convert_token(const DecodeArgs& p, int t, char* dst, float* s_sc
   __syncthreads();
 }
 
-// Single token: this thread's 16-byte chunks of x and of the shared-expert gate, loaded
-// into registers before the weight stream starts so that they are not queued behind it.
 // One token: warps 1..15 (kConvThreads threads, named barrier 1) load x and the shared
 // gate vector, reduce max|x| and the gate dot product, and write x' = x / 2^s (max|x'| in
 // [256, 512)) as a padded f16 row, while warp 0 obtains the routing slots.
@@ -754,8 +756,9 @@ __device__ __forceinline__ void dequant_row(const uint4& q, uint32_t (&w)[16]) {
 // filled by per-lane cp.async (each lane copies its own 16 code bytes of both rows and 4
 // scale bytes; one commit group per slot), with a header naming the step's unit and
 // k-step. The issue side runs up to kDecodeDepth steps ahead of the compute side and
-// crosses unit boundaries freely. start() only issues the first copies: it runs before
-// whatever the phase waits for (the activations, the grid barrier), so the weights are in
+// crosses unit boundaries freely. start() only issues the first copies, as early as the
+// weights are known (W2: before the grid barrier, one token: as soon as the warp's W13
+// units are done; W13 of several tokens: before the activation conversion), so they are in
 // flight when run() begins.
 template <int NT, int MODE>
 struct PhaseStream {
@@ -1103,9 +1106,10 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   if (NT == 1 && tid < 32) finish_plan_t1(p, P, t1r);
   const int n_routed = P.misc[2];
 
-  // activations: every CTA converts all tokens into its shared memory (small T), or the
-  // CTAs convert one token each into a shared global copy (larger T), then a grid barrier
-  if (NT == 1) {   // x converted before the plan; thread 0 wrote misc[4] in finish_plan_t1
+  // activations: one token was converted before the plan (x_t1_convert); several tokens:
+  // every CTA converts all tokens into its shared memory (small T), or the CTAs convert
+  // one token each into a shared global copy (larger T), then a grid barrier
+  if (NT == 1) {   // thread 0 wrote misc[4] in finish_plan_t1
     if (tid == 0) {
       P.xscale[0] = s_scale;
       if (has_shared)
