@@ -58,7 +58,15 @@ PREFILL_T2048 = LayerSpec("prefill_t2048_e512_k10_h4096_i1024", seed=4, T=2048, 
                           prefill=True)
 
 WORKLOADS = [TINY, DECODE_B1_E288, DECODE_B1_E512, DECODE_B32_E512, PREFILL_T2048]
-BY_NAME = {s.name: s for s in WORKLOADS}
+
+# Further decode shapes between and beside those: a mid-size batch of the 512-expert layer,
+# and a layer with few, large experts (a long reduction per weight row).
+DECODE_B8_E512 = LayerSpec("decode_t8_e512_k10_h4096_i1024_shared", seed=5, T=8, E=512, k=10,
+                           H=4096, I=1024, logit_sigma=1.5, shared=True, instances=4)
+DECODE_B1_DEEP = LayerSpec("decode_t1_e8_k2_h8192_i4096", seed=6, T=1, E=8, k=2, H=8192,
+                           I=4096, logit_sigma=1.0, instances=8)
+EXTRA_WORKLOADS = [DECODE_B8_E512, DECODE_B1_DEEP]
+BY_NAME = {s.name: s for s in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def gen_x(spec: LayerSpec, instance: int = 0) -> np.ndarray:

@@ -7,7 +7,8 @@ import pytest
 import torch
 
 from oracle import moe as om
-from synth import DECODE_B1_E288, DECODE_B1_E512, DECODE_B32_E512, LayerSpec, make_layer
+from synth import (DECODE_B1_DEEP, DECODE_B1_E288, DECODE_B1_E512, DECODE_B8_E512,
+                   DECODE_B32_E512, LayerSpec, make_layer)
 from synth.device import HostExperts, make_device_layer, nvfp4_experts
 from synth import philox as px
 from tests.layer_util import assert_close, bf16_to_f64, ftmoe
@@ -62,3 +63,13 @@ def test_full_decode_t1_e512_shared_other_instance():
 
 def test_full_decode_t32_e512_shared_sampled():
     _device_parity(DECODE_B32_E512, tokens=np.array([0, 9, 17, 31]))
+
+
+def test_full_decode_t8_e512_shared_sampled():
+    """Mid-size decode batch of the 512-expert layer."""
+    _device_parity(DECODE_B8_E512, tokens=np.array([0, 3, 7]))
+
+
+def test_full_decode_t1_few_large_experts():
+    """Few, large experts: H = 8192, I = 4096 (eight k-steps per W13 row, four per W2 row)."""
+    _device_parity(DECODE_B1_DEEP)

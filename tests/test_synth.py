@@ -95,7 +95,9 @@ def test_workload_shapes_and_logit_bias():
 
 
 def test_workload_table():
+    from synth.workload import BY_NAME, EXTRA_WORKLOADS
     names = [w.name for w in WORKLOADS]
     assert len(set(names)) == 5
-    for w in WORKLOADS:
+    assert len(BY_NAME) == len(WORKLOADS) + len(EXTRA_WORKLOADS)
+    for w in WORKLOADS + EXTRA_WORKLOADS:
         assert w.H % 128 == 0 and w.I % 128 == 0 and w.k <= w.E
