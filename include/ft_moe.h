@@ -107,6 +107,12 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                               int32_t has_shared, int32_t prefill);
 
+/* Dynamic shared memory per CTA that the decode kernel launches with for these sizes (one
+ * CTA per SM, 512 threads): the plan, the activations when they are kept on chip, and the
+ * weight rings. Host-only arithmetic, no device call; 0 for sizes decode does not accept. */
+size_t ft_moe_decode_smem_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                                int32_t has_shared);
+
 /* Zero a workspace once after allocating it (the error word and the reduction counters
  * must start at zero; every call leaves them at zero again). Enqueued on `stream`. */
 ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -135,6 +135,15 @@ size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_
   return PrefillLayout(T, k, E, H, I, has_shared != 0).total;
 }
 
+size_t ft_moe_decode_smem_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                                int32_t has_shared) {
+  if (T < 1 || T > kMaxDecodeT || k < 1 || k > kMaxTopK || E < 1 || E > kMaxExperts || k > E ||
+      H < 1 || I < 1 || H % 128 != 0 || I % 128 != 0 || H > 16384 || I > 8192)
+    return 0;
+  const size_t need = DecodeSmem(T, k, E, H, I, has_shared != 0).total;
+  return need > kDecodeSmem ? need : kDecodeSmem;
+}
+
 ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes == 0) return FT_ERR_INVALID_ARG;
   return cuda_status(

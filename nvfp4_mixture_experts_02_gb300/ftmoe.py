@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_UNSUPPORTED_SHAP
 EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_workspace_bytes",
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
             "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
-            "ft_moe_nvfp4_decode_routed"]
+            "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes"]
 
 
 class FtError(RuntimeError):
@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ft_moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     lib.ft_moe_workspace_bytes.restype = sz
     lib.ft_moe_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.ft_moe_decode_smem_bytes.restype = sz
+    lib.ft_moe_decode_smem_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.ft_moe_workspace_init.restype = ctypes.c_int
     lib.ft_moe_workspace_init.argtypes = [vp, sz, vp]
     layer = [vp, i32, vp, vp, i32, ctypes.POINTER(_Experts), ctypes.POINTER(_Shared), f32,

@@ -116,3 +116,24 @@ def test_empty_batch_is_a_no_op(lib):
     # the shape checks still apply to an empty batch
     assert f.ft_moe_nvfp4_decode(None, 0, None, None, 9, ctypes.byref(ex), None, 7.0, None,
                                  None, 0, None) == 1
+
+
+def test_decode_shared_memory_fits_every_accepted_shape(lib):
+    """Every shape decode accepts (T <= 64, k <= 32, E <= 4096, H <= 16384, I <= 8192) fits
+    the kernel's 224 KB of shared memory per CTA: the plan, x when kept on chip, the rings."""
+    f = lib.lib().ft_moe_decode_smem_bytes
+    budget = 224 * 1024
+    worst = 0
+    for T in (1, 2, 5, 8, 16, 32, 33, 63, 64):
+        for k in (1, 2, 8, 10, 16, 32):
+            for E in (32, 64, 288, 512, 1024, 2048, 4096):
+                if k > E:
+                    continue
+                for H in (128, 256, 512, 1024, 4096, 16384):
+                    for I in (128, 1024, 8192):
+                        for sh in (0, 1):
+                            n = f(T, k, E, H, I, sh)
+                            assert 0 < n <= budget, (T, k, E, H, I, sh, n)
+                            worst = max(worst, n)
+    assert worst == budget   # the launch asks for the whole budget
+    assert f(65, 2, 8, 256, 128, 0) == 0 and f(1, 33, 64, 256, 128, 0) == 0
