@@ -129,6 +129,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -157,6 +167,19 @@ __device__ __forceinline__ void dequant64(const uint4& q0, const uint4& q1, uint
   const uint32_t s[4] = {splat_lo(s01), splat_hi(s01), splat_lo(s23), splat_hi(s23)};
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = hmul2(r[i], s[i >> 3]);   // 8 words per 16-element block
+}
+
+// 32 elements of one row (16 packed bytes + 2 E4M3 block scales, low byte first) -> 16
+// f16x2 words holding e2m1 * e4m3 exactly; word i = elements 2i and 2i+1.
+__device__ __forceinline__ void dequant32(const uint4& q, uint32_t sc2, uint32_t (&r)[16]) {
+  e2m1x8_to_f16x2x4(q.x, r[0], r[1], r[2], r[3]);
+  e2m1x8_to_f16x2x4(q.y, r[4], r[5], r[6], r[7]);
+  e2m1x8_to_f16x2x4(q.z, r[8], r[9], r[10], r[11]);
+  e2m1x8_to_f16x2x4(q.w, r[12], r[13], r[14], r[15]);
+  const uint32_t s01 = e4m3x2_to_f16x2(sc2 & 0xFFFFu);
+  const uint32_t s[2] = {splat_lo(s01), splat_hi(s01)};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = hmul2(r[i], s[i >> 3]);   // 8 words per 16-element block
 }
 
 // Byte offset of the 16-byte piece j (k = 8j..8j+7) of row n in a K-major, no-swizzle tile

@@ -11,15 +11,16 @@
 //   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
 //                           part[pair], in slot order (deterministic), bf16 out
 //
-// k_pf_gemm is persistent (one CTA per SM, 8 producer warps and one MMA warp). A work
+// k_pf_gemm is persistent (one CTA per SM, 16 producer warps and one MMA warp). A work
 // item is one token group of one expert (up to 128 tokens, the MMA N) against 256 weight
 // rows: for W13 the 128 gate rows and the 128 matching up rows of a row block (two fp32
 // accumulators in tensor memory, so SwiGLU pairs land in the same TMEM lane), for W2 two
 // 128-row blocks of the output. The item's weight codes arrive as tiles of 4 chunks (256
 // rows x 128 bytes) through the tensor-memory-access engine (two 2D tensor-map copies per
 // tile, 128-byte swizzle, three tile slots), sent by the MMA warp once every producer is
-// past the tile the slot held. Each producer thread owns one weight row: it reads its
-// row's 32 code bytes of a chunk from the tile, takes the E4M3 scales through a small
+// past the tile the slot held. Two producer threads share each weight row, each owning
+// half of every chunk (32 elements): it reads its 16 code bytes from the tile, takes its two
+// E4M3 scales through a small
 // register pipeline (L1-allocating loads), forms e2m1*e4m3 exactly in f16 (hardware
 // conversions + one f16x2 multiply per pair) and writes it into tensor memory
 // (tcgen05.st) as the MMA's A operand. The group's activations (B operand) go straight from global to shared memory
@@ -43,7 +44,7 @@ namespace ftmoe {
 
 namespace {
 
-constexpr int kPfProducers = 256;        // 8 producer warps: rows 0-127 of set 0 / set 1
+constexpr int kPfProducers = 512;        // 16 producer warps: two threads per weight row
 constexpr int kPfThreads = kPfProducers + 32;   // + one warp that issues the MMAs
 constexpr int kPfN = 128;                // max tokens per group (MMA N)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
@@ -351,6 +352,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool producer = tid < kPfProducers;
   const int set = (warp >> 2) & 1;           // row set 0 / 1 (producers)
+  const int half = (warp >> 3) & 1;          // which 32 elements of a chunk (producers)
   const int m = (warp & 3) * 32 + lane;      // row inside the set = TMEM lane
   unsigned char* sB = pf_smem;               // [kPfBStages][kBTileBytes]
   const uint32_t sW = smem_addr(pf_smem + kPfBStages * kBTileBytes);   // [kPfWTiles][2 sets][128][128 B]
@@ -437,14 +439,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     (void)wrow;
     uint32_t sc[kPfStages];
     auto issue = [&](int d, int c) {
-      sc[d] = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(srow + (size_t)c * 4)) : 0u;
+      sc[d] = row_ok ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(srow + (size_t)c * 4) + half)
+                     : 0u;
     };
     // the group's activation tile of chunk c straight into shared-memory stage bst
     // (cp.async, no registers; padding rows n >= nv are zero-filled): one commit group
     auto issue_b = [&](int c, int bst) {
       const uint32_t bt = smem_addr(sB + bst * kBTileBytes);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < kPfN * 8 / kPfProducers; ++r) {
         const int i = tid + r * kPfProducers;
         if (i < npad * 8) {
           const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
@@ -522,10 +525,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
           tc_fence_after();
           if (c + kPfStages < nchunks) issue_b(c + kPfStages, (int)((nprod + kPfStages) % kPfBStages));
           else cp_async_commit();
-          uint32_t r[32];
-          dequant64(lds_v4(rbase + (((2 * d) ^ sw) << 4)), lds_v4(rbase + (((2 * d + 1) ^ sw) << 4)),
-                    sc[d], r);
-          tmem_st32(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32, r);
+          uint32_t r[16];
+          dequant32(lds_v4(rbase + (((2 * d + half) ^ sw) << 4)), sc[d], r);
+          tmem_st16(tbase + lane_off + kColA + (uint32_t)(st * 2 + set) * 32 + (uint32_t)half * 16, r);
           if (c + kPfStages < nchunks) issue(d, c + kPfStages);
           cp_async_wait<kPfStages>();   // this chunk's activation tile has landed
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -545,10 +547,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     tc_fence_after();
     if (ok && producer) {
       if (kW13) {
-        // warps 0-3 and 4-7 share the lanes; split the columns in blocks of 16
+        // four warps share each lane quarter (set 0 / 1, half 0 / 1): columns in blocks of 16
         const float g13 = e >= 0 ? __ldg(p.g13 + e) : __ldg(p.sh_g13);
         const int i_out = rb * 128 + m;
-        for (int nb = set * 16; nb < npad; nb += 32) {
+        for (int nb = (set + 2 * half) * 16; nb < npad; nb += 64) {
           uint32_t gv[16], uv[16];
           tmem_ld16(tbase + lane_off + kColD0 + nb, gv);
           tmem_ld16(tbase + lane_off + kColD1 + nb, uv);
@@ -567,7 +569,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         const float oscale = __int_as_float(p.hdr[3]) * p.oscale_mul;
         const int r_out = rb * 256 + set * 128 + m;
         const uint32_t dcol = set == 0 ? kColD0 : kColD1;
-        for (int nb = 0; nb < npad; nb += 16) {
+        for (int nb = half * 16; nb < npad; nb += 32) {
           uint32_t dv[16];
           tmem_ld16(tbase + lane_off + dcol + nb, dv);
 #pragma unroll
