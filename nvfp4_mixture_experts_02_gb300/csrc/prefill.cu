@@ -11,26 +11,24 @@
 //   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
 //                           part[pair], in slot order (deterministic), bf16 out
 //
-// k_pf_gemm is persistent (one CTA per SM, 16 producer warps and one MMA warp). A work
-// item is one token group of one expert (up to 128 tokens, the MMA N) against 256 weight
-// rows: for W13 the 128 gate rows and the 128 matching up rows of a row block (two fp32
-// accumulators in tensor memory, so SwiGLU pairs land in the same TMEM lane), for W2 two
-// 128-row blocks of the output. The item's weight codes arrive as tiles of 4 chunks (256
-// rows x 128 bytes) through the tensor-memory-access engine (two 2D tensor-map copies per
-// tile, 128-byte swizzle, three tile slots), sent by the MMA warp once every producer is
-// past the tile the slot held. Two producer threads share each weight row, each owning
-// half of every chunk (32 elements): it reads its 16 code bytes from the tile, takes its two
-// E4M3 scales through a small
-// register pipeline (L1-allocating loads), forms e2m1*e4m3 exactly in f16 (hardware
-// conversions + one f16x2 multiply per pair) and writes it into tensor memory
-// (tcgen05.st) as the MMA's A operand. The group's activations (B operand) go straight from global to shared memory
-// by cp.async, in the canonical K-major core-matrix layout, 4 chunks ahead in 8 stages.
-// Every producer arrives on the stage's "full" mbarrier when its part of a chunk is in
-// place; the MMA warp waits for the stage and, as a whole converged warp with one elected
-// lane, issues tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group
-// size rounded up to 16, K=16 per instruction), committing to the stage's "done"
-// mbarrier. Four stages and no CTA-wide barrier per chunk let the producers run ahead of
-// the MMAs.
+// k_pf_gemm is persistent (one CTA per SM, 16 producer warps and one MMA warp). A work item is
+// one token group of one expert (up to 128 tokens, the MMA N) against 256 weight rows: for W13
+// the 128 gate rows and the 128 matching up rows of a row block (two fp32 accumulators in
+// tensor memory, so SwiGLU pairs land in the same TMEM lane), for W2 two 128-row blocks of the
+// output. The item's weight codes arrive as tiles of 4 chunks (256 rows x 128 bytes) through
+// the tensor-memory-access engine (two 2D tensor-map copies per tile, 128-byte swizzle, three
+// tile slots), sent by the MMA warp once every producer is past the tile the slot held. Two
+// producer threads share each weight row, each owning half of every chunk (32 elements): it
+// reads its 16 code bytes from the tile, takes its two E4M3 scales through a small register
+// pipeline (L1-allocating loads), forms e2m1*e4m3 exactly in f16 (hardware conversions + one
+// f16x2 multiply per pair) and writes it into tensor memory (tcgen05.st) as the MMA's A
+// operand. The group's activations (B operand) go straight from global to shared memory by
+// cp.async, in the canonical K-major core-matrix layout, 4 chunks ahead in 8 stages. Every
+// producer arrives on the stage's "full" mbarrier when its part of a chunk is in place; the MMA
+// warp waits for the stage and, as a whole converged warp with one elected lane, issues
+// tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group size rounded up
+// to 16, K=16 per instruction), committing to the stage's "done" mbarrier. Four stages and no
+// CTA-wide barrier per chunk let the producers run ahead of the MMAs.
 #include <cmath>
 #include <cstdint>
 #include <cuda.h>          // CUtensorMap (the encoder is fetched through the runtime)
