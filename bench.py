@@ -349,16 +349,22 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     torch.cuda.synchronize()
 
     def one(i, b):
+        if nb == 1:   # on the current stream: no per-step stream switch on the host
+            _one(i, b)
+            return
         with torch.cuda.stream(streams[b]):
-            dins[b].copy_(hin[i], non_blocking=True)
-            if spec.prefill:
-                ftmoe.route(dls[b], spec.k, idxs[b], wts[b])
-                call(dxs[b], idxs[b], wts[b], exps[i], shs[i], limit=spec.swiglu_limit,
-                     out=outs[b], workspace=wss[b])
-            else:   # the routed decode call (one launch for one token)
-                ftmoe.decode_routed(dxs[b], dls[b], spec.k, exps[i], shs[i],
-                                    limit=spec.swiglu_limit, out=outs[b], workspace=wss[b])
-            houts[b].copy_(outs[b].view(torch.int16), non_blocking=True)
+            _one(i, b)
+
+    def _one(i, b):
+        dins[b].copy_(hin[i], non_blocking=True)
+        if spec.prefill:
+            ftmoe.route(dls[b], spec.k, idxs[b], wts[b])
+            call(dxs[b], idxs[b], wts[b], exps[i], shs[i], limit=spec.swiglu_limit,
+                 out=outs[b], workspace=wss[b])
+        else:   # the routed decode call (one launch for one token)
+            ftmoe.decode_routed(dxs[b], dls[b], spec.k, exps[i], shs[i],
+                                limit=spec.swiglu_limit, out=outs[b], workspace=wss[b])
+        houts[b].copy_(outs[b].view(torch.int16), non_blocking=True)
 
     for i in range(min(n, 4)):
         one(i, i % nb)
@@ -367,12 +373,14 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
-    for st in streams:
-        st.wait_stream(main)
+    if nb > 1:
+        for st in streams:
+            st.wait_stream(main)
     for s_ in range(steps):
         one(s_ % n, s_ % nb)
-    for st in streams:
-        main.wait_stream(st)
+    if nb > 1:
+        for st in streams:
+            main.wait_stream(st)
     e1.record(main)
     torch.cuda.synchronize()
     for w_ in wss:
