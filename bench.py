@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--instances", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unrouted", action="store_true",
+                    help="one-token decode as ft_moe_route + ft_moe_nvfp4_decode (two launches) "
+                         "instead of the routed call; the roofline then times the decode launch")
     return ap.parse_args()
 
 
@@ -181,7 +184,7 @@ def run_ours(args, spec, rank, world, local):
     call = ftmoe.prefill if prefill else ftmoe.decode
     # one-token decode: the routed call is one launch (the kernel routes the token itself),
     # so the call and the expert kernel are the same launch
-    fused = not prefill and spec.T == 1
+    fused = not prefill and spec.T == 1 and not getattr(args, "unrouted", False)
 
     def step(i, with_route=True):
         lay = layers[i]
@@ -357,7 +360,7 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
 
     def _one(i, b):
         dins[b].copy_(hin[i], non_blocking=True)
-        if spec.prefill:
+        if spec.prefill or getattr(args, "unrouted", False):
             ftmoe.route(dls[b], spec.k, idxs[b], wts[b])
             call(dxs[b], idxs[b], wts[b], exps[i], shs[i], limit=spec.swiglu_limit,
                  out=outs[b], workspace=wss[b])
