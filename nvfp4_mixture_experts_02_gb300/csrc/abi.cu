@@ -1,6 +1,7 @@
 // C ABI of the library: argument checks, workspace sizing and dispatch to the kernels.
 // Every check runs on the host before anything is enqueued.
 #include <cmath>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
@@ -15,17 +16,17 @@ namespace {
 
 constexpr int32_t kAbiVersion = 1;
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices] = {0};  // per-device attribute cache
+std::atomic<int> g_sm_count[kMaxDevices];  // per-device attribute cache (0: not read yet)
 
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 thread_local cudaError_t t_last_cuda = cudaSuccess;

@@ -34,6 +34,7 @@
 // given device.
 //
 // Every device-side wait is bounded and reports FT_ERR_TIMEOUT instead of hanging.
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -1357,22 +1358,24 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   const bool t1 = decode_nt(T) == 1;
   const int vi = t1 ? 0 : 1;
   constexpr int kDevs = 64;
-  static size_t smem_set[kDevs][2] = {};
-  static bool pdl_off[kDevs] = {};
+  // per-device caches, safe under concurrent host threads (setting the attribute twice is
+  // harmless: every launch of a kernel variant asks for the same size, kDecodeSmem)
+  static std::atomic<size_t> smem_set[kDevs][2];
+  static std::atomic<bool> pdl_off[kDevs];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
-  if (smem > smem_set[dev][vi]) {
+  if (smem > smem_set[dev][vi].load(std::memory_order_relaxed)) {
     err = t1 ? cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem)
              : cudaFuncSetAttribute(k_decode<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem);
     if (err != cudaSuccess) return err;
-    smem_set[dev][vi] = smem;
+    smem_set[dev][vi].store(smem, std::memory_order_relaxed);
   }
   for (int attempt = 0; attempt < 2; ++attempt) {
-    const bool pdl = !pdl_off[dev];
+    const bool pdl = !pdl_off[dev].load(std::memory_order_relaxed);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(32 * decode_warps(T));
@@ -1388,7 +1391,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
     err = t1 ? cudaLaunchKernelEx(&cfg, k_decode<1>, a) : cudaLaunchKernelEx(&cfg, k_decode<4>, a);
     if (err == cudaSuccess || !pdl) return err;
     (void)cudaGetLastError();   // cooperative + programmatic serialization refused
-    pdl_off[dev] = true;
+    pdl_off[dev].store(true, std::memory_order_relaxed);
   }
   return err;
 }

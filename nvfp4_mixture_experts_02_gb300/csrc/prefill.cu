@@ -29,6 +29,7 @@
 // tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group size rounded up
 // to 16, K=16 per instruction), committing to the stage's "done" mbarrier. Four stages and no
 // CTA-wide barrier per chunk let the producers run ahead of the MMAs.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda.h>          // CUtensorMap (the encoder is fetched through the runtime)
@@ -672,7 +673,8 @@ PrefillLayout::PrefillLayout(int T, int k, int E, int H, int I, bool shared) {
 // 128-byte swizzle, zero fill past the tensor (rows past an expert read the next expert's,
 // which only ever land in rows whose results are dropped).
 bool code_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = cached.load(std::memory_order_acquire);
   if (encode == nullptr) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -681,6 +683,7 @@ bool code_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
         q != cudaDriverEntryPointSuccess || fn == nullptr)
       return false;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cached.store(encode, std::memory_order_release);
   }
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
@@ -727,11 +730,11 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
     if ((err = cudaLaunchKernelEx(&cfg, k_pf_act, aa)) != cudaSuccess) return err;
   }
   const size_t smem = (size_t)kPfBStages * kBTileBytes + (size_t)kPfWTiles * kWTileBytes;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // per device; setting twice is harmless
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_relaxed)) {
     // one CTA per SM (the kernel takes all 512 TMEM columns): ask for enough shared memory
     // that a second CTA cannot be co-resident
     const int want = smem > 120 * 1024 ? (int)smem : 120 * 1024;
@@ -741,7 +744,7 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
     if ((err = cudaFuncSetAttribute(k_pf_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     want)) != cudaSuccess)
       return err;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_relaxed);
   }
   const size_t smem_launch = smem > 120 * 1024 ? smem : 120 * 1024;
   PfGemmArgs g;
