@@ -97,12 +97,19 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
   asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// Grid barrier on a monotonic 64-bit arrival counter: barrier b of a launch completes when
-// the counter reaches base + (b + 1) * gridDim.x, base = its value when the launch began
-// (every launch adds gridDim.x per barrier, so base is a multiple of it). Arrival (one
-// release add per CTA) and waiting are separate calls, so a CTA can start streaming the
-// next phase's weights in between; the wait is bounded.
+// Grid barrier on a monotonic 64-bit arrival counter: barrier n (1, 2, ...) of a launch
+// completes when the counter reaches base + n * gridDim.x, base = its value when the launch
+// began (every launch adds gridDim.x per barrier, so base is a multiple of it). Thread 0 of
+// each CTA reads the counter at any point before its CTA's first arrival: fewer than
+// gridDim.x arrivals of this launch can precede that read, so rounding it down to whole
+// grids gives base. Arrival (one release add per CTA) and waiting are separate calls, so a
+// CTA can start streaming the next phase's weights in between; the wait is bounded.
 __device__ void grid_arrive(unsigned long long* bar) {
   __syncthreads();
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
@@ -627,30 +634,33 @@ __device__ __forceinline__ void phase_shape(const DecodeArgs& p, const Plan& P, 
 // Cut of a phase's units into CTA ranges of equal cost. With `weighted`, a unit of segment
 // s costs step_cost(tokens of s), else 1. CTA v's range starts at the first unit whose cost
 // start reaches floor(Ctot * v / G), evaluated as q * v + floor(r * v / G) with
-// Ctot = q * G + r, so no 64-bit division is needed (r * v < G^2).
+// Ctot = q * G + r. All of it fits 32-bit unsigned arithmetic (a 64-bit division is a long
+// software sequence on the plan's critical path): Ctot <= J * (cost of every pair in a
+// segment of its own) <= 8192 * (64 * 33) * step_cost(1) < 2^27 for every accepted shape,
+// and r * v < G^2.
 struct UnitMap {
-  int J, n_seg, G, weighted, r;
-  long long U, Ctot, q;
+  int J, n_seg, G, weighted;
+  unsigned U, Ctot, q, r;
 
-  __device__ __forceinline__ void set_total(long long total) {
+  __device__ __forceinline__ void set_total(unsigned total) {
     Ctot = total;
-    q = total / G;
-    r = (int)(total - q * G);
+    q = total / (unsigned)G;
+    r = total - q * (unsigned)G;
   }
-  __device__ __forceinline__ long long cost_lo(int v) const {
-    return q * v + (int)((unsigned)(r * v) / (unsigned)G);
+  __device__ __forceinline__ unsigned cost_lo(int v) const {
+    return q * (unsigned)v + r * (unsigned)v / (unsigned)G;
   }
   __device__ int first_unit(const Plan& P, int v) const {
     if (v >= G) return (int)U;
-    const long long L = cost_lo(v);
+    const unsigned L = cost_lo(v);
     if (!weighted) return (int)L;
     int lo = 0, hi = n_seg;   // largest seg < n_seg with J * cp[seg] <= L
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if ((long long)J * P.seg_cp[mid] <= L) lo = mid;
+      if ((unsigned)J * (unsigned)P.seg_cp[mid] <= L) lo = mid;
       else hi = mid;
     }
-    const int rem = (int)(L - (long long)J * P.seg_cp[lo]);
+    const int rem = (int)(L - (unsigned)J * (unsigned)P.seg_cp[lo]);
     const int c = step_cost(P.seg_pair0[lo + 1] - P.seg_pair0[lo]);
     const int k = (rem + c - 1) / c;
     return k >= J ? (lo + 1) * J : lo * J + k;
@@ -663,8 +673,8 @@ __device__ void cta_units(const DecodeArgs& p, const Plan& P, int& lo, int& hi) 
   int U, J, S;
   phase_shape<MODE>(p, P, U, J, S);
   if (MODE == kW2Rows) {   // whole row pairs per CTA, all experts of each
-    lo = (int)((long long)J * blockIdx.x / gridDim.x) * P.misc[0];
-    hi = (int)((long long)J * (blockIdx.x + 1) / gridDim.x) * P.misc[0];
+    lo = (int)((unsigned)J * blockIdx.x / gridDim.x) * P.misc[0];
+    hi = (int)((unsigned)J * (blockIdx.x + 1) / gridDim.x) * P.misc[0];
     return;
   }
   UnitMap m;
@@ -672,10 +682,10 @@ __device__ void cta_units(const DecodeArgs& p, const Plan& P, int& lo, int& hi) 
   m.n_seg = P.misc[5];
   m.G = gridDim.x;
   m.weighted = NT > 1;
-  m.U = U;
+  m.U = (unsigned)U;
   lo = hi = 0;
   if (U == 0) return;
-  m.set_total(m.weighted ? (long long)J * P.seg_cp[m.n_seg] : (long long)U);
+  m.set_total(m.weighted ? (unsigned)J * (unsigned)P.seg_cp[m.n_seg] : (unsigned)U);
   lo = m.first_unit(P, blockIdx.x);
   hi = m.first_unit(P, blockIdx.x + 1);
 }
@@ -1053,14 +1063,20 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   griddep_launch_dependents();
   griddep_wait();   // routing results may come from the previous kernel
 
-  // barrier targets: the arrival counter as this launch began, rounded down to whole grids
-  __shared__ unsigned long long s_base;
-  if (tid == 0) s_base = ld_acquire64(p.bar) / gridDim.x * gridDim.x;
+  // the grid barrier's base count (thread 0 only): read now by a relaxed load (it only
+  // fixes a count; the waits synchronise) whose latency stays off the routing and the plan,
+  // and rounded down to whole grids (a 64-bit division) by round_base() at a point where no
+  // other warp waits for thread 0, before the first wait
+  unsigned long long bar_base = 0;
+  if (tid == 0) bar_base = ld_relaxed64(p.bar);
+  auto round_base = [&]() {
+    if (tid == 0) bar_base = bar_base / gridDim.x * gridDim.x;
+  };
   int n_bar = 0;
   auto arrive = [&]() { grid_arrive(p.bar); };
   auto wait = [&]() {
     ++n_bar;
-    grid_wait(p.bar, s_base + (unsigned long long)n_bar * gridDim.x, p.err);
+    grid_wait(p.bar, bar_base + (unsigned long long)n_bar * gridDim.x, p.err);
   };
 
   const bool has_shared = p.sh_g13 != nullptr;
@@ -1106,6 +1122,9 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   w13s.start(p, P, ring, &s_disp[0], s_range[1]);
   if (NT == 1 && tid < 32) finish_plan_t1(p, P, t1r);
   const int n_routed = P.misc[2];
+
+  const bool early_wait = NT > 1 && !x_on_chip;   // the conversion below waits at the barrier
+  if (early_wait) round_base();
 
   // activations: one token was converted before the plan (x_t1_convert); several tokens:
   // every CTA converts all tokens into its shared memory (small T), or the CTAs convert
@@ -1155,6 +1174,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   const bool up13_smem = NT == 1 && n13 <= stage_cap;
   float2* upart = up13_smem ? reinterpret_cast<float2*>(stage)
                             : p.upart + (size_t)blockIdx.x * p.upart_units * 8;
+  if (!early_wait) round_base();   // only warp 0 starts its units later; the others take them
   w13s.run(p, P, a13, upart, s_range[0]);
   // One token: this warp's W13 units are done and its ring is empty, so its W2 weight
   // copies go out now, while the CTA's other warps finish their last W13 units (the W2
