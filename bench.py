@@ -1,10 +1,11 @@
 """Benchmark of the NVFP4 MoE layer on GB300: one JSON line on stdout (rank 0).
 
-A step is one layer call: router (ft_moe_route) + experts (ft_moe_nvfp4_decode, or
-ft_moe_nvfp4_prefill for the prefill workload) on one synthetic layer instance. The
-decode workloads rotate over 48 distinct instances (weights far larger than L2, so every
-call streams its experts from HBM); the timed loop replays a CUDA graph of one pass over
-the instances.
+A step is one layer call on one synthetic layer instance: for one token the routed decode
+(ft_moe_nvfp4_decode_routed, routing inside the one launch); for several tokens the router
+(ft_moe_route) + experts (ft_moe_nvfp4_decode, or ft_moe_nvfp4_prefill for the prefill
+workload). The decode workloads rotate over distinct instances (weights far larger than L2,
+so every call streams its experts from HBM). Exactly K steps are timed: CUDA graphs of whole
+passes over the instances, then one of the remaining steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -299,7 +300,7 @@ def run_ours(args, spec, rank, world, local):
         "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k, "H": spec.H,
                    "I": spec.I, "shared_expert": spec.shared, "instances": n_inst,
                    "l2": f"inputs larger than L2: {n_inst} distinct layer instances rotated",
-                   "graph": "CUDA graph of one pass over the instances",
+                   "graph": "CUDA graphs: whole passes over the instances, then the rest",
                    "bytes_per_call": round(bytes_call), "experts_touched_mean":
                    statistics.mean(touched)},
         "roofline": roof, "e2e": e2e,
