@@ -1,8 +1,10 @@
-"""Thin ctypes binding of libftmoe.so (include/ft_moe.h): argument marshalling only.
+"""Thin ctypes binding of libftmoe.so (include/ft_moe.h): argument checks and marshalling.
 
 Every step of the layer runs in the library's CUDA kernels. torch supplies device
 memory and streams; there is no CPU fallback, and importing this module without the
-built library raises.
+built library raises. Tensors are checked before their pointers are handed over (device,
+element type, contiguity, shape): the expert objects once when built, the per-call tensors
+on every call.
 """
 from __future__ import annotations
 
@@ -92,9 +94,12 @@ def _ptr(t) -> int:
     return 0 if t is None else t.data_ptr()
 
 
-def _stream(stream) -> int:
+def _stream(stream, dev=None) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
+    if dev is not None and stream.device_index != dev:
+        raise ValueError(f"the tensors are on cuda:{dev}, the stream on cuda:{stream.device_index} "
+                         "(torch.cuda.set_device selects the current device)")
     return stream.cuda_stream
 
 
@@ -104,16 +109,68 @@ def _check(st: int, what: str):
         raise FtError(st, what, detail)
 
 
-@dataclass
+# The kernels reach every tensor through its raw pointer, so a host tensor, a narrower
+# element type, a strided view or a wrong shape would be read or written out of bounds on
+# the GPU. _need refuses those before the call (a few hundred ns per tensor); the expert
+# tensors are checked once, when their objects are built.
+BF16_BITS = (torch.bfloat16, torch.int16, torch.uint16)   # bf16 values or their bit patterns
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+
+
+def _need(t, name, dev, dtypes, shape):
+    """t on cuda:dev, of one of `dtypes` (None: any 1-byte type), contiguous, of `shape`
+    (None: any)."""
+    if t.get_device() != dev:
+        raise ValueError(f"{name}: expected a tensor on cuda:{dev}, got one on {t.device}")
+    if (t.element_size() != 1) if dtypes is None else (t.dtype not in dtypes):
+        raise TypeError(f"{name}: element type {t.dtype} is not accepted here")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: the tensor must be contiguous")
+    if shape is not None and t.shape != shape:
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _need_scalar(t, name, dev):
+    _need(t, name, dev, _F32, None)
+    if t.numel() != 1:
+        raise ValueError(f"{name}: one float32 value expected, got {t.numel()}")
+
+
+def _device_of(t, what) -> int:
+    dev = t.get_device()
+    if dev < 0:
+        raise ValueError(f"{what}: CUDA tensors are required, got one on {t.device}")
+    return dev
+
+
+@dataclass(frozen=True)
 class NvFP4Experts:
     """Routed experts on the device: w13 u8 [E,2I,H/2], s13 u8 [E,2I,H/16], g13 f32 [E],
-    w2 u8 [E,H,I/2], s2 u8 [E,H,I/16], g2 f32 [E]."""
+    w2 u8 [E,H,I/2], s2 u8 [E,H,I/16], g2 f32 [E] (codes and scales: any 1-byte type).
+    Checked when built: one device, contiguous, consistent shapes."""
     w13: torch.Tensor
     s13: torch.Tensor
     g13: torch.Tensor
     w2: torch.Tensor
     s2: torch.Tensor
     g2: torch.Tensor
+
+    def __post_init__(self):
+        dev = _device_of(self.w13, "NvFP4Experts")
+        if self.w13.dim() != 3 or self.w2.dim() != 3:
+            raise ValueError("NvFP4Experts: w13 [E,2I,H/2] and w2 [E,H,I/2] are 3-D")
+        E, H, I = self.E, self.H, self.I
+        _need(self.w13, "w13", dev, None, (E, 2 * I, H // 2))
+        _need(self.s13, "s13", dev, None, (E, 2 * I, H // 16))
+        _need(self.g13, "g13", dev, _F32, (E,))
+        _need(self.w2, "w2", dev, None, (E, H, I // 2))
+        _need(self.s2, "s2", dev, None, (E, H, I // 16))
+        _need(self.g2, "g2", dev, _F32, (E,))
+        object.__setattr__(self, "device_index", dev)
+        object.__setattr__(self, "_cs", _Experts(E, H, I, _ptr(self.w13), _ptr(self.s13),
+                                                 _ptr(self.g13), _ptr(self.w2), _ptr(self.s2),
+                                                 _ptr(self.g2)))
 
     @property
     def E(self):
@@ -128,14 +185,14 @@ class NvFP4Experts:
         return self.w13.shape[1] // 2
 
     def cstruct(self) -> _Experts:
-        return _Experts(self.E, self.H, self.I, _ptr(self.w13), _ptr(self.s13), _ptr(self.g13),
-                        _ptr(self.w2), _ptr(self.s2), _ptr(self.g2))
+        return self._cs
 
 
-@dataclass
+@dataclass(frozen=True)
 class NvFP4Shared:
-    """Shared expert on the device (no E dimension); g13/g2 are 1-element f32 tensors and
-    gate is bf16 [H] (any 16-bit dtype holding the bf16 bits)."""
+    """Shared expert on the device (no E dimension): w13 [2I,H/2], s13 [2I,H/16], w2 [H,I/2],
+    s2 [H,I/16] (any 1-byte type), g13/g2 1-element f32 tensors and gate bf16 [H] (or a
+    16-bit integer tensor holding the bf16 bits). Checked when built."""
     w13: torch.Tensor
     s13: torch.Tensor
     g13: torch.Tensor
@@ -144,9 +201,31 @@ class NvFP4Shared:
     g2: torch.Tensor
     gate: torch.Tensor
 
+    def __post_init__(self):
+        dev = _device_of(self.w13, "NvFP4Shared")
+        if self.w13.dim() != 2 or self.w2.dim() != 2:
+            raise ValueError("NvFP4Shared: w13 [2I,H/2] and w2 [H,I/2] are 2-D")
+        H, I = self.w2.shape[0], self.w13.shape[0] // 2
+        _need(self.w13, "shared w13", dev, None, (2 * I, H // 2))
+        _need(self.s13, "shared s13", dev, None, (2 * I, H // 16))
+        _need(self.w2, "shared w2", dev, None, (H, I // 2))
+        _need(self.s2, "shared s2", dev, None, (H, I // 16))
+        _need_scalar(self.g13, "shared g13", dev)
+        _need_scalar(self.g2, "shared g2", dev)
+        _need(self.gate, "shared gate", dev, BF16_BITS, (H,))
+        object.__setattr__(self, "device_index", dev)
+        object.__setattr__(self, "H", H)
+        object.__setattr__(self, "I", I)
+        object.__setattr__(self, "_cs", _Shared(_ptr(self.w13), _ptr(self.s13), _ptr(self.g13),
+                                                _ptr(self.w2), _ptr(self.s2), _ptr(self.g2),
+                                                _ptr(self.gate)))
+
+    def check_for(self, experts: NvFP4Experts):
+        if (self.device_index, self.H, self.I) != (experts.device_index, experts.H, experts.I):
+            raise ValueError("shared expert: H, I and the device must match the routed experts")
+
     def cstruct(self) -> _Shared:
-        return _Shared(_ptr(self.w13), _ptr(self.s13), _ptr(self.g13), _ptr(self.w2),
-                       _ptr(self.s2), _ptr(self.g2), _ptr(self.gate))
+        return self._cs
 
 
 def abi_version() -> int:
@@ -159,12 +238,21 @@ def status_string(st: int) -> str:
 
 def route(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, stream=None):
     """ft_moe_route on fp32 logits [T, E] (device). Returns (idx int32 [T,k], w f32 [T,k])."""
+    dev = _device_of(logits, "ft_moe_route")
+    if logits.dim() != 2:
+        raise ValueError("logits: [T, E] expected")
+    _need(logits, "logits", dev, _F32, None)
     T, E = logits.shape
     if topk_idx is None:
         topk_idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    else:
+        _need(topk_idx, "topk_idx", dev, _I32, (T, k))
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
-    st = _LIB.ft_moe_route(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    else:
+        _need(topk_w, "topk_w", dev, _F32, (T, k))
+    st = _LIB.ft_moe_route(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w),
+                           _stream(stream, dev))
     _check(st, "ft_moe_route")
     return topk_idx, topk_w
 
@@ -187,16 +275,43 @@ def new_workspace(T, k, experts: NvFP4Experts, has_shared, prefill=False, device
     return ws
 
 
-def _layer(fn, name, x, topk_idx, topk_w, experts, shared, limit, out, workspace, stream):
+def _call_tensors(experts, shared, x, out, workspace, T_name="x"):
+    """Checks shared by the layer calls: x [T,H] and out [T,H] (bf16 bits), the shared expert
+    against the routed ones, the workspace (1-byte elements: numel() is its size in bytes).
+    Returns (device, T, out)."""
+    dev = experts.device_index
+    if x.dim() != 2:
+        raise ValueError(f"{T_name}: [T, H] expected")
     T = x.shape[0]
-    k = topk_idx.shape[1]
+    _need(x, T_name, dev, BF16_BITS, (T, experts.H))
+    if shared is not None:
+        shared.check_for(experts)
     if out is None:
         out = torch.empty((T, experts.H), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", dev, BF16_BITS, (T, experts.H))
+    if workspace is not None:
+        _need(workspace, "workspace", dev, None, None)
+    return dev, T, out
+
+
+def _slots(topk_idx, topk_w, T, dev):
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx: [T, k] expected")
+    k = topk_idx.shape[1]
+    _need(topk_idx, "topk_idx", dev, _I32, (T, k))
+    _need(topk_w, "topk_w", dev, _F32, (T, k))
+    return k
+
+
+def _layer(fn, name, x, topk_idx, topk_w, experts, shared, limit, out, workspace, stream):
+    dev, T, out = _call_tensors(experts, shared, x, out, workspace)
+    k = _slots(topk_idx, topk_w, T, dev)
     ex = experts.cstruct()
     sh = shared.cstruct() if shared is not None else None
     st = fn(_ptr(x), T, _ptr(topk_idx), _ptr(topk_w), k, ctypes.byref(ex),
             ctypes.byref(sh) if sh is not None else None, float(limit), _ptr(out),
-            _ptr(workspace), workspace.numel(), _stream(stream))
+            _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st, name)
     return out
 
@@ -215,15 +330,14 @@ def decode_noalloc(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=Non
                    stream=None):
     """ft_moe_nvfp4_decode_noalloc: decode with the library's fixed scratch array (no
     workspace, no device allocation by the library)."""
-    T, k = x.shape[0], topk_idx.shape[1]
-    if out is None:
-        out = torch.empty((T, experts.H), dtype=torch.bfloat16, device=x.device)
+    dev, T, out = _call_tensors(experts, shared, x, out, None)
+    k = _slots(topk_idx, topk_w, T, dev)
     ex = experts.cstruct()
     sh = shared.cstruct() if shared is not None else None
     st = _LIB.ft_moe_nvfp4_decode_noalloc(_ptr(x), T, _ptr(topk_idx), _ptr(topk_w), k,
                                           ctypes.byref(ex),
                                           ctypes.byref(sh) if sh is not None else None,
-                                          float(limit), _ptr(out), _stream(stream))
+                                          float(limit), _ptr(out), _stream(stream, dev))
     _check(st, "ft_moe_nvfp4_decode_noalloc")
     return out
 
@@ -232,17 +346,20 @@ def decode_routed(x, logits, k, experts, shared=None, limit=7.0, out=None, topk_
                   topk_w=None, workspace=None, stream=None):
     """ft_moe_nvfp4_decode_routed: the layer from the router logits f32 [T,E] (T <= 64); one
     launch for T = 1. topk_idx / topk_w (int32 / f32 [T,k]), when given, receive the slots."""
-    T = x.shape[0]
     if workspace is None:
-        workspace = new_workspace(T, k, experts, shared is not None, stream=stream)
-    if out is None:
-        out = torch.empty((T, experts.H), dtype=torch.bfloat16, device=x.device)
+        workspace = new_workspace(x.shape[0], k, experts, shared is not None, stream=stream)
+    dev, T, out = _call_tensors(experts, shared, x, out, workspace)
+    _need(logits, "logits", dev, _F32, (T, experts.E))
+    if topk_idx is not None:
+        _need(topk_idx, "topk_idx", dev, _I32, (T, k))
+    if topk_w is not None:
+        _need(topk_w, "topk_w", dev, _F32, (T, k))
     ex = experts.cstruct()
     sh = shared.cstruct() if shared is not None else None
     st = _LIB.ft_moe_nvfp4_decode_routed(_ptr(x), T, _ptr(logits), k, ctypes.byref(ex),
                                          ctypes.byref(sh) if sh is not None else None,
                                          float(limit), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
-                                         _ptr(workspace), workspace.numel(), _stream(stream))
+                                         _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st, "ft_moe_nvfp4_decode_routed")
     return out
 
@@ -258,4 +375,5 @@ def prefill(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, work
 
 
 def get_error(workspace, stream=None) -> int:
-    return _LIB.ft_moe_get_error(_ptr(workspace), _stream(stream))
+    dev = _device_of(workspace, "ft_moe_get_error")
+    return _LIB.ft_moe_get_error(_ptr(workspace), _stream(stream, dev))
