@@ -137,3 +137,38 @@ def test_decode_shared_memory_fits_every_accepted_shape(lib):
                             worst = max(worst, n)
     assert worst == budget   # the launch asks for the whole budget
     assert f(65, 2, 8, 256, 128, 0) == 0 and f(1, 33, 64, 256, 128, 0) == 0
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "ft_moe.h"
+int main(void) {
+  /* host-side calls only: the version, a status string, a workspace size and an argument
+     error that is returned before anything touches a GPU */
+  ft_status st = ft_moe_route(NULL, 1, 8, 2, NULL, NULL, NULL);
+  printf("%d|%s|%zu|%d\n", ft_moe_abi_version(), ft_status_string(FT_ERR_MISALIGNED),
+         ft_moe_workspace_bytes(1, 2, 8, 256, 128, 0, 0), (int)st);
+  return st == FT_ERR_INVALID_ARG ? 0 : 1;
+}
+"""
+
+
+def test_header_serves_a_plain_c_caller(lib, tmp_path):
+    """include/ft_moe.h compiles as strict C11 and a C program links and calls the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src, exe = tmp_path / "caller.c", tmp_path / "caller"
+    src.write_text(C_CALLER)
+    libdir = os.path.dirname(lib.LIB_PATH)
+    res = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                          "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lftmoe",
+                          f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, run.stdout + run.stderr
+    version, status, ws, st = run.stdout.strip().split("|")
+    assert int(version) == lib.abi_version() and status.startswith("FT_ERR_MISALIGNED")
+    assert int(ws) == lib.workspace_bytes(1, 2, 8, 256, 128, False) and int(st) == 1
