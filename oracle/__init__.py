@@ -7,6 +7,7 @@ it, and has no CPU fallback.
 
 Modules
 * ``oracle.nvfp4`` — E2M1 / E4M3 / bf16 decoding and NVFP4 dequantisation.
+* ``oracle.fp8block`` — block-FP8 dequantisation (E4M3 elements, float32 tile scales).
 * ``oracle.moe``   — route (softmax, top-k, renormalise), clamped SwiGLU experts, the
   router-weighted sum and the gated shared expert.
 
@@ -15,4 +16,4 @@ oracle: the printed E2M1 value table, the library float8 type, hand-derived clos
 forms stored under tests/golden/, brute force on tiny inputs, and invariants (weights sum
 to one, a zero expert contributes nothing, linearity in W2, the k = E dense reduction).
 """
-from . import moe, nvfp4  # noqa: F401
+from . import fp8block, moe, nvfp4  # noqa: F401

@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from .fp8block import dequantize_fp8_block
 from .nvfp4 import bf16_bits_to_f32, dequantize
 
 
@@ -63,13 +64,23 @@ def clamped_swiglu(g: np.ndarray, u: np.ndarray, limit: float) -> np.ndarray:
     return (silu(np.minimum(g, L)) * np.clip(u, -L, L)).astype(np.float32)
 
 
-def expert_forward(xs: np.ndarray, w13, s13, g13, w2, s2, g2, limit: float) -> np.ndarray:
+def weights(codes, scales, gscale, fmt: str) -> np.ndarray:
+    """One expert projection as float32 [rows, K]: NVFP4 (packed codes, E4M3 block scales,
+    tensor scale) or block-FP8 (E4M3 codes, float32 tile scales; no tensor scale)."""
+    if fmt == "fp8block":
+        return dequantize_fp8_block(codes, scales)
+    assert fmt == "nvfp4", fmt
+    return dequantize(codes, scales, gscale)
+
+
+def expert_forward(xs: np.ndarray, w13, s13, g13, w2, s2, g2, limit: float,
+                   fmt: str = "nvfp4") -> np.ndarray:
     """One expert on a batch of token rows xs float32 [n, H] -> float32 [n, H]."""
-    W13 = dequantize(w13, s13, g13)                 # [2I, H]
+    W13 = weights(w13, s13, g13, fmt)               # [2I, H]
     I = W13.shape[0] // 2
     gu = xs @ W13.T                                 # [n, 2I] float32
     h = clamped_swiglu(gu[:, :I], gu[:, I:], limit)
-    W2 = dequantize(w2, s2, g2)                     # [H, I]
+    W2 = weights(w2, s2, g2, fmt)                   # [H, I]
     return (h @ W2.T).astype(np.float32)
 
 
@@ -79,11 +90,12 @@ def sigmoid(z):
 
 
 def moe_layer(x_bits, logits, k: int, experts, shared=None, limit: float = 7.0,
-              tokens=None):
+              tokens=None, fmt: str = "nvfp4"):
     """The whole layer for the token rows ``tokens`` (default: all).
 
     ``experts`` is anything with attributes w13, s13, g13, w2, s2, g2 that can be indexed
-    by expert id (numpy arrays, or a lazy accessor that fetches one expert at a time).
+    by expert id (numpy arrays, or a lazy accessor that fetches one expert at a time); for
+    block-FP8 (``fmt="fp8block"``) g13 and g2 are unused and may be None.
     ``shared`` is None or a dict with keys w13 s13 g13 w2 s2 g2 gate.
     Returns (y float32 [n, H], idx int32 [n, k], w float32 [n, k]).
     """
@@ -98,13 +110,15 @@ def moe_layer(x_bits, logits, k: int, experts, shared=None, limit: float = 7.0,
     for j in range(k):                               # slot order: sum_j w_tj * E_tj(x_t)
         for e in np.unique(idx[:, j]):
             rows = np.nonzero(idx[:, j] == e)[0]
-            out = expert_forward(x[rows], experts.w13[e], experts.s13[e], experts.g13[e],
-                                 experts.w2[e], experts.s2[e], experts.g2[e], limit)
+            g13 = None if experts.g13 is None else experts.g13[e]
+            g2 = None if experts.g2 is None else experts.g2[e]
+            out = expert_forward(x[rows], experts.w13[e], experts.s13[e], g13,
+                                 experts.w2[e], experts.s2[e], g2, limit, fmt)
             y[rows] += w[rows, j][:, None] * out
     if shared is not None:
         gv = bf16_bits_to_f32(shared["gate"])
         s = sigmoid(x @ gv)                           # [n] float32
         out = expert_forward(x, shared["w13"], shared["s13"], shared["g13"],
-                             shared["w2"], shared["s2"], shared["g2"], limit)
+                             shared["w2"], shared["s2"], shared["g2"], limit, fmt)
         y += s[:, None] * out
     return y, idx, w

@@ -1,4 +1,5 @@
-"""NVFP4 quantiser used to make the synthetic expert weights.
+"""Quantisers used to make the synthetic expert weights (NVFP4, and block-FP8 for the
+other routed-expert format).
 
 The layer receives its weights already quantised; quantisation is how the synthetic
 inputs are made, so it lives with the input generators and not with the layer.
@@ -103,6 +104,40 @@ def quantize_nvfp4(w: np.ndarray):
     codes = codes.reshape(rows, K)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     return packed, scales.astype(np.uint8), g
+
+
+FP8_BLOCK = 128
+
+
+def quantize_fp8_block(w: np.ndarray, block: int = FP8_BLOCK):
+    """Block-FP8: one float32 scale per block x block tile of w [rows, K] (the last tile
+    row and column ragged when a dimension is not a multiple of the block) and one E4M3
+    code per element.
+
+    * block scale   s = block_amax / 448                       (float32 division)
+    * element code  E4M3 round-to-nearest-even of |w| / s, saturating at 448, with the
+                    sign in bit 7 (kept for values that round to zero)
+    A tile whose amax is zero gets scale 0 and all-zero codes.
+
+    Returns (codes uint8 [rows, K], scales float32 [ceil(rows/block), ceil(K/block)]).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    rows, K = w.shape
+    nr, nk = -(-rows // block), -(-K // block)
+    scales = np.zeros((nr, nk), dtype=np.float32)
+    codes = np.zeros((rows, K), dtype=np.uint8)
+    for i in range(nr):
+        for j in range(nk):
+            tile = w[i * block:(i + 1) * block, j * block:(j + 1) * block]
+            amax = np.float32(np.max(np.abs(tile)))
+            if amax == 0.0:
+                continue
+            sc = np.float32(amax / np.float32(448.0))
+            scales[i, j] = sc
+            mag = e4m3_encode((np.abs(tile) / sc).astype(np.float32))
+            sign = np.signbit(tile).astype(np.uint8) << 7
+            codes[i * block:(i + 1) * block, j * block:(j + 1) * block] = mag | sign
+    return codes, scales
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -21,7 +21,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 from . import philox as px
-from .quantize import f32_to_bf16_bits, quantize_nvfp4
+from .quantize import f32_to_bf16_bits, quantize_fp8_block, quantize_nvfp4
 
 
 @dataclass(frozen=True)
@@ -41,6 +41,7 @@ class LayerSpec:
     x_sigma: float = 1.0
     swiglu_limit: float = 7.0
     prefill: bool = False
+    fmt: str = "nvfp4"            # expert weight format: "nvfp4" or "fp8block"
 
 
 # The five workloads of the layer (shapes as stated for the MoE layer under test).
@@ -99,9 +100,15 @@ def gen_w2_fp32(spec: LayerSpec, instance: int, e: int, tid: int = px.TID_W2):
 
 
 def gen_expert(spec: LayerSpec, instance: int, e: int, shared: bool = False):
-    """Quantised weights of one expert: (w13, s13, g13, w2, s2, g2)."""
+    """Quantised weights of one expert: (w13, s13, g13, w2, s2, g2). Block-FP8 has no
+    tensor scale: g13 and g2 are None, s13 and s2 are the float32 block scales."""
     t13 = px.TID_W13_SHARED if shared else px.TID_W13
     t2 = px.TID_W2_SHARED if shared else px.TID_W2
+    if spec.fmt == "fp8block":
+        w13, s13 = quantize_fp8_block(gen_w13_fp32(spec, instance, e, t13))
+        w2, s2 = quantize_fp8_block(gen_w2_fp32(spec, instance, e, t2))
+        return w13, s13, None, w2, s2, None
+    assert spec.fmt == "nvfp4", spec.fmt
     w13, s13, g13 = quantize_nvfp4(gen_w13_fp32(spec, instance, e, t13))
     w2, s2, g2 = quantize_nvfp4(gen_w2_fp32(spec, instance, e, t2))
     return w13, s13, g13, w2, s2, g2
@@ -125,19 +132,13 @@ class Layer:
 
 def make_layer(spec: LayerSpec, instance: int = 0) -> Layer:
     """Generate a whole layer on the host. Meant for the small shapes (seconds of CPU)."""
-    E, H, I = spec.E, spec.H, spec.I
-    w13 = np.empty((E, 2 * I, H // 2), np.uint8)
-    s13 = np.empty((E, 2 * I, H // 16), np.uint8)
-    g13 = np.empty(E, np.float32)
-    w2 = np.empty((E, H, I // 2), np.uint8)
-    s2 = np.empty((E, H, I // 16), np.uint8)
-    g2 = np.empty(E, np.float32)
-    for e in range(E):
-        w13[e], s13[e], g13[e], w2[e], s2[e], g2[e] = gen_expert(spec, instance, e)
+    per = [gen_expert(spec, instance, e) for e in range(spec.E)]
+    w13, s13, g13, w2, s2, g2 = (
+        None if per[0][i] is None else np.stack([p[i] for p in per]) for i in range(6))
     shared = None
     if spec.shared:
         a, b, c, d, f, g = gen_expert(spec, instance, 0, shared=True)
-        shared = dict(w13=a, s13=b, g13=np.float32(c), w2=d, s2=f, g2=np.float32(g),
-                      gate=gen_gate(spec, instance))
+        shared = dict(w13=a, s13=b, g13=None if c is None else np.float32(c), w2=d, s2=f,
+                      g2=None if g is None else np.float32(g), gate=gen_gate(spec, instance))
     return Layer(spec, gen_x(spec, instance), gen_logits(spec, instance),
                  w13, s13, g13, w2, s2, g2, shared)
