@@ -293,14 +293,16 @@ def run_ours(args, spec, rank, world, local):
         "us_per_call": round(us_call, 3), "tokens_per_s": round(spec.T * steps_done * world /
                                                                  (step_ms * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("nvfp4 weights (e2m1 x e4m3), f16 tcgen05 mma, f32 accumulate, bf16 in/out"
-                  if prefill else "nvfp4 weights (e2m1 x e4m3), f16x2 fma per 16-element block, "
-                  "f32 accumulate, bf16 in/out"),
+        "dtype": "nvfp4/f16/f32",
         "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, N(0,1) bf16 x)",
         "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k, "H": spec.H,
                    "I": spec.I, "shared_expert": spec.shared, "instances": n_inst,
                    "l2": f"inputs larger than L2: {n_inst} distinct layer instances rotated",
                    "graph": "CUDA graphs: whole passes over the instances, then the rest",
+                   "arith": ("NVFP4 weights (e2m1 x e4m3) as exact f16 products, f16 tcgen05 MMA, "
+                             "f32 accumulate, bf16 in/out" if prefill else
+                             "NVFP4 weights (e2m1 x e4m3), f16x2 FMA per 16-element block, "
+                             "f32 accumulate, bf16 in/out"),
                    "bytes_per_call": round(bytes_call), "experts_touched_mean":
                    statistics.mean(touched)},
         "roofline": roof, "e2e": e2e,
@@ -469,7 +471,7 @@ def run_reference(args, spec, rank, world, local):
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": per_call * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32 (oracle)", "data": "synthetic",
+            "dtype": "f32", "data": "synthetic",
             "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k,
                        "H": spec.H, "I": spec.I, "shared_expert": spec.shared},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
