@@ -161,7 +161,7 @@ ft_status ft_moe_nvfp4_decode(const uint16_t* x, int32_t T, const int32_t* topk_
   if (st != FT_OK || T == 0) return st;
   if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
   // smallest possible workspace first (no CUDA call), then the exact one for this device
-  if (workspace_bytes < DecodeLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr, 1).total)
+  if (workspace_bytes < DecodeLayout::lower_bound(T, k, ex->E, ex->H, ex->I, sh != nullptr))
     return FT_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count();
   if (sms <= 0) return FT_ERR_CUDA;
@@ -187,7 +187,7 @@ ft_status ft_moe_nvfp4_decode_routed(const uint16_t* x, int32_t T, const float* 
       !aligned(topk_idx_out, 4) || !aligned(topk_w_out, 4))
     return FT_ERR_MISALIGNED;
   if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
-  if (workspace_bytes < DecodeLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr, 1).total)
+  if (workspace_bytes < DecodeLayout::lower_bound(T, k, ex->E, ex->H, ex->I, sh != nullptr))
     return FT_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count();
   if (sms <= 0) return FT_ERR_CUDA;

@@ -1282,8 +1282,18 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   max_pairs = T * k + (shared ? T : 0);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  // the head (error word, barrier counter, completion counters) must be zero before a call;
+  // every call leaves it at zero again
   err = take(16);
   bar = take(16);
+  ready = take(4 * (kMaxTopK + 2));
+  t1 = T == 1 && d1_geom(H, I, grid).ok;
+  if (t1) {   // one token: the SwiGLU outputs of every active slot, nothing else
+    xf = take(0);
+    h = take((size_t)(k + 1) * I * 2);
+    total = o;
+    return;
+  }
   const bool x_on_chip = DecodeSmem(T, k, E, H, I, shared).x_on_chip;
   xf = take(x_on_chip ? 16 : (size_t)T * decode_act_row_bytes(H));   // shared copy
   xscale = take(sizeof(float) * 2 * (size_t)T);
@@ -1296,6 +1306,13 @@ DecodeLayout::DecodeLayout(int T, int k, int E, int H, int I, bool shared, int g
   part = take(T > 1 ? sizeof(float) * (size_t)max_pairs * H : 16);
   topk = take(8 * (size_t)T * k);
   total = o;
+}
+
+size_t DecodeLayout::lower_bound(int T, int k, int E, int H, int I, bool shared) {
+  const size_t general = DecodeLayout(T, k, E, H, I, shared, 1).total;
+  if (T != 1) return general;
+  const size_t t1 = 3 * 256 + align_up((size_t)(k + 1) * I * 2, 256);   // head + h
+  return t1 < general ? t1 : general;
 }
 
 __host__ __device__ DecodeSmem::DecodeSmem(int T, int k, int E, int H, int I, bool shared) {
@@ -1351,6 +1368,9 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   int S = -40;
   while (S < 24 && (double)limit * limit * std::ldexp(1.0, S + 1) <= 512.0) ++S;
   const float hscale = (float)std::ldexp(1.0, S);
+  if (WL.t1)
+    return launch_decode1(x, topk_idx, topk_w, k, ex, limit, hscale, out, ws, WL, grid,
+                          1u << 22, stream, logits, topk_idx_out, topk_w_out);
 
   DecodeArgs a;
   a.x = x; a.T = T; a.k = k; a.E = ex.E; a.H = ex.H; a.I = ex.I;

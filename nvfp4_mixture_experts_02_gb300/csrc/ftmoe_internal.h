@@ -30,6 +30,13 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
                           int num_sms, cudaStream_t stream, const float* logits = nullptr,
                           int* topk_idx_out = nullptr, float* topk_w_out = nullptr);
 
+// The one-token kernel (decode1.cu) for a workspace laid out by DecodeLayout with t1 set.
+cudaError_t launch_decode1(const uint16_t* x, const int* topk_idx, const float* topk_w, int k,
+                           const ExpertPtrs& ex, float limit, float hscale, uint16_t* out,
+                           void* ws, const DecodeLayout& WL, int grid, unsigned spin_limit,
+                           cudaStream_t stream, const float* logits, int* topk_idx_out,
+                           float* topk_w_out);
+
 // Workspace regions of the prefill path (byte offsets, 256-byte aligned).
 struct PrefillLayout {
   int max_pairs = 0, max_groups = 0;

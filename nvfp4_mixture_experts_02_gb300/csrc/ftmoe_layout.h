@@ -16,6 +16,31 @@ constexpr int kDecodeDepth = 6;                // decode: weight steps in flight
 constexpr int kDecodeSlot = 1232;              // one step: 2 x 512 codes, 2 x 96 scales, header
 constexpr int kDecodePtrTable = 512;           // decode: largest plan with a pointer table
 
+// One-token decode kernel (decode1.cu): ring stages and warps.
+constexpr int kD1MaxStages = 16;
+constexpr int kD1TabStages = 64;   // stages whose copies are laid out in advance
+constexpr int kD1Warps = 20;   // 16 consumers, stage issuer, W13 finisher, h issuer, publisher
+#ifndef FTMOE_D1_CHUNK_CAP
+#define FTMOE_D1_CHUNK_CAP 4
+#endif
+constexpr int kD1ChunkCap = FTMOE_D1_CHUNK_CAP;   // 512-element chunks per warp K-segment
+constexpr size_t kD1SmemMax = 232448;         // dynamic shared memory of one CTA (227 KB)
+
+// Geometry of the one-token kernel for one shape and grid (host-computed, passed to the kernel).
+struct D1Geom {
+  int ok = 0;
+  int nseg13 = 1, kseg13 = 0, xc13 = 0;   // W13 rows: K-segments, elements and chunks of one
+  int pps = 0, sps = 0;                   // W13 stage: row pairs, stages per active slot
+  int nseg2 = 1, kseg2 = 0, xc2 = 0;      // W2 rows: K-segments
+  int n2max = 0, rw = 0, w2runs = 0, rb = 0;   // W2: rows per CTA (max), rows per run, runs per
+                                               // stage, bytes per run
+  int w13_stage = 0, slot_bytes = 0, ns = 0;   // ring
+  int variant = 0;   // kernel instance: chunk counts fixed at compile time, or checked
+  int off_bar = 0, off_pf = 0, off_cand = 0, off_misc = 0, off_act = 0, off_yacc = 0,
+      off_tab = 0, off_sched = 0, off_ring = 0, smem = 0;
+};
+D1Geom d1_geom(int H, int I, int grid);
+
 // Error word bits (workspace offset 0).
 constexpr int kErrBadExpert = 1;
 constexpr int kErrTimeout = 2;
@@ -45,10 +70,16 @@ struct DecodeLayout {
   int max_act = 0;     // active experts (routed, distinct) + shared
   int max_pairs = 0;   // (token, expert) pairs incl. the shared expert's T pairs
   int upart_units = 0;   // units per CTA slice of the one-token partial sums
-  size_t err = 0, bar = 0, xf = 0, xscale = 0, h = 0, upart = 0, part = 0,
+  bool t1 = false;     // one token through the bulk-copy kernel (decode1.cu)
+  size_t err = 0, bar = 0,
+         ready = 0,   // one token: per-slot W13 completion counters + CTA count (zero between calls)
+         xf = 0, xscale = 0, h = 0, upart = 0, part = 0,
          topk = 0,   // routed decode of several tokens: the routing slots [T][k] idx, then w
          total = 0;
   DecodeLayout(int T, int k, int E, int H, int I, bool shared, int grid);
+  // A size no decode workspace of these sizes is below on any grid (host check before the
+  // device is queried).
+  static size_t lower_bound(int T, int k, int E, int H, int I, bool shared);
 };
 
 // Shared-memory carve-up of the decode kernel (same code on host and device).
