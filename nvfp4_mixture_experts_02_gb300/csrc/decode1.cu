@@ -40,11 +40,12 @@
 //   is stored in f16 pre-multiplied by the router weight, the ratio of its W2 tensor scale to a
 //   per-call reference, and 2^S (2^S * L^2 <= 512), as in the several-token kernel.
 //
-// * Routing (routed call, E <= 512): each consumer warp takes the local top-k of 32 logits (k
-//   rounds of a warp-wide max and ballot, ties to the lowest lane = the lower expert), then
-//   warp 0 merges the 16 sorted lists (k rounds over the list heads, ties to the lower list) and
-//   forms the weights with the route kernel's own warp routine, so the experts and weights are
-//   bit-identical to ft_moe_route. Beyond 512 experts warp 0 runs the route kernel's routine.
+// * Routing (routed call, E <= 512) by counting, without serial rounds: in each consumer warp
+//   every lane counts the lanes that beat its logit (larger, or equal with a lower expert id);
+//   the warp's k best become candidates, each of which counts the candidates that beat it, and
+//   the k best take their slots. Warp 0 then forms the weights with the route kernel's own warp
+//   routine, so the experts and weights are bit-identical to ft_moe_route. Beyond 512 experts
+//   warp 0 runs the route kernel's routine.
 //
 // Every output row is summed in a fixed order (slot by slot, K-segment by K-segment), so the
 // bits are reproducible. Every device wait is bounded; a wait on other CTAs that runs out sets
@@ -328,7 +329,7 @@ __device__ __forceinline__ void row_dot(uint32_t ca, uint32_t sa, const uint32_t
 struct Sm {
   uint32_t full, empty;   // [kD1MaxStages] mbarriers each
   uint32_t pf;            // [ns][16] float2: (gate, up) partial sums per consumer warp
-  uint32_t cand;          // [16][32] routing candidates: key, expert, logit (3 arrays)
+  uint32_t cand;          // routing: candidates (u64 keys, experts, logits), then the k slots
   uint32_t red;           // [32] float: max |x| per warp, then gate-dot partials
   uint32_t misc;          // [0] stages armed by the issuer [1] W13 stages finished
   uint32_t scal;          // [0] activation scale [1] W2 reference scale
@@ -373,7 +374,7 @@ struct W13Stage {
 };
 __device__ __forceinline__ W13Stage w13_stage(const Sm& S, const D1Geom& g, int v, int G, int s) {
   W13Stage t;
-  t.ws = s / g.sps;
+  t.ws = g.sps == 1 ? s : s / g.sps;
   const int part = s - t.ws * g.sps;
   int pos = v + t.ws;
   while (pos >= G) pos -= G;
@@ -395,7 +396,7 @@ struct StageLayout {
   int ncp, ws, j0, n;
   StageCopy cp[8];
 };
-__device__ __forceinline__ StageLayout stage_layout(const Sm& S, const D1Geom& g, int v, int G,
+__device__ __noinline__ StageLayout stage_layout(const Sm& S, const D1Geom& g, int v, int G,
                                                     int s, int S13, int n2, int r0, int rps,
                                                     int n_runs, int H, int I) {
   StageLayout L;
@@ -444,43 +445,40 @@ __device__ __forceinline__ W13Stage w13_info(const Sm& S, const D1Geom& g, int v
 }
 
 // ------------------------------------------------------------------------ routing
-// Local top-k of one warp's 32 logits (E <= 512): k rounds of a warp max over the keys not yet
-// picked, the lowest lane among equal keys (= the lower expert). Picks are stored in order.
+// Routing by counting (E <= 512), with no serial rounds. An expert's place in the ranking is the
+// number of experts that beat it: a larger logit key, or an equal key and a lower expert id.
+// Step 1: in each warp, every lane counts the lanes of its 32 that beat it; the k best of the
+// warp become candidates, stored as 64-bit words (key << 32 | ~candidate index) so that one
+// unsigned comparison is the ranking rule (candidates are stored warp by warp and, within a warp,
+// by local rank, i.e. in expert order among equal keys).
 __device__ __forceinline__ void route_local(const Sm& S, unsigned key, float v, int e, int k,
                                             int warp, int lane) {
-  bool live = true;
-  for (int r = 0; r < k; ++r) {
-    const unsigned m = __reduce_max_sync(0xffffffffu, live ? key : 0u);
-    const unsigned b = __ballot_sync(0xffffffffu, live && key == m);
-    if (lane == __ffs(b) - 1) {
-      live = false;
-      const uint32_t at = 4 * (warp * 32 + r);
-      sts32(S.cand + at, key);
-      sts32(S.cand + 2048 + at, (uint32_t)e);
-      stsf(S.cand + 4096 + at, v);
-    }
+  int rank = 0;
+#pragma unroll 8
+  for (int d = 1; d < 32; ++d) {
+    const int o = (lane + d) & 31;
+    const unsigned ko = __shfl_sync(0xffffffffu, key, o);
+    rank += (ko > key) || (ko == key && o < lane);
+  }
+  if (rank < k) {
+    const uint32_t c = (uint32_t)(warp * k + rank);
+    stsu64(S.cand + 8 * c, ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - c));
+    sts32(S.cand + 4096 + 4 * c, (uint32_t)e);
+    stsf(S.cand + 4096 + 2048 + 4 * c, v);
   }
 }
 
-// Warp 0: merge the 16 sorted lists (list j holds experts of [32j, 32j + 32)): k rounds of the
-// largest head key, ties to the lowest list. Lane r < k ends with slot r's expert and logit.
-__device__ void route_merge(const Sm& S, int k, int lane, int& out_e, float& out_v) {
-  int pos = 0;
-  unsigned hk = lane < kCW ? lds32(S.cand + 4 * (lane * 32)) : 0u;
-  for (int r = 0; r < k; ++r) {
-    const unsigned m = __reduce_max_sync(0xffffffffu, hk);
-    const unsigned b = __ballot_sync(0xffffffffu, lane < kCW && hk == m);
-    const int win = __ffs(b) - 1;
-    const int wpos = __shfl_sync(0xffffffffu, pos, win);
-    if (lane == r) {
-      const uint32_t at = 4 * (win * 32 + wpos);
-      out_e = ldsi(S.cand + 2048 + at);
-      out_v = ldsf(S.cand + 4096 + at);
-    }
-    if (lane == win) {
-      ++pos;
-      hk = pos < k ? lds32(S.cand + 4 * (lane * 32 + pos)) : 0u;
-    }
+// Step 2: candidate c (thread c < 16 k) counts the candidates that beat it; the k best take
+// their slots: slot r = (expert, logit) at cand + 8192 + 8 r.
+__device__ __forceinline__ void route_rank(const Sm& S, int k, int tid) {
+  const int nc = kCW * k;
+  if (tid >= nc) return;
+  const uint64_t me = ldsu64(S.cand + 8 * tid);
+  int rank = 0;
+  for (int c = 0; c < nc; ++c) rank += ldsu64(S.cand + 8 * c) > me;
+  if (rank < k) {
+    sts32(S.cand + 8192 + 8 * rank, lds32(S.cand + 4096 + 4 * tid));
+    sts32(S.cand + 8192 + 8 * rank + 4, lds32(S.cand + 4096 + 2048 + 4 * tid));
   }
 }
 
@@ -562,8 +560,12 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       stsf(S.red + 4 * warp, amax);
       stsf(S.red + 4 * (16 + warp), dot);
     }
-    if (routed && p.E <= 512) route_local(S, key, lv, e, k, warp, lane);
-    consumer_sync();   // (A) x staged, partials and routing candidates in shared memory
+    if (routed && p.E <= 512) {
+      route_local(S, key, lv, e, k, warp, lane);
+      consumer_sync();
+      route_rank(S, k, tid);
+    }
+    consumer_sync();   // (A) x staged, partials and the routing slots in shared memory
 
     // ---- warp 0: the slots; every warp: its activations, scaled, into registers
     if (warp == 0) {
@@ -572,10 +574,13 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       if (routed) {
         if (p.E <= 512) {
           float v0 = 0.f;
-          route_merge(S, k, lane, e_in, v0);
+          if (lane < k) {
+            e_in = ldsi(S.cand + 8192 + 8 * lane);
+            v0 = ldsf(S.cand + 8192 + 8 * lane + 4);
+          }
           w_in = route_weights(v0, k, lane);
         } else {
-          route_warp_any(p.logits, p.E, k, lane, e_in, w_in);
+          route_warp_wide(p.logits, p.E, k, lane, e_in, w_in);
         }
         if (lane >= k) e_in = -1;
         if (v == 0 && lane < k) {
@@ -674,12 +679,13 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     __syncwarp();
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      int slot = 0;
+      uint32_t ph = 0;   // ring slot of stage s and the parity of its use of the slot
       for (int s = 0; s < S13 + S2; ++s) {
-        const int slot = s % g.ns;
         const uint32_t full = S.full + 8 * slot;
         if (s >= g.ns) {   // the slot's previous stage released by its consumers and, for
           const int old = s - g.ns;   // W13, its partial sums read by the finisher
-          mb_wait(S.empty + 8 * slot, (old / g.ns) & 1, p.err);
+          mb_wait(S.empty + 8 * slot, ph ^ 1u, p.err);
           if (old < S13)
             for (uint32_t it = 0; (int)lds_flag(S.misc + 4) <= old; ++it) {
               if (it > kMbarSpin) {
@@ -707,6 +713,10 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
                 L.cp[c].bytes, full, pol);
         }
         sts_flag(S.misc, (uint32_t)(s + 1));   // stage s armed
+        if (++slot == g.ns) {
+          slot = 0;
+          ph ^= 1u;
+        }
       }
       // no copy may still be landing when the CTA exits: wait for the last stage of every
       // slot (the consumers have normally seen them all already)
@@ -757,9 +767,9 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       __syncwarp();
     }
     const float xscale = ldsf(S.scal);
+    int slot = 0;
+    uint32_t par = 0;
     for (int s = 0; s < S13; ++s) {
-      const int slot = s % g.ns;
-      const uint32_t par = (s / g.ns) & 1;
       if (lane == 0) mb_wait_sleep(S.empty + 8 * slot, par, p.err);
       __syncwarp();
       (void)mb_try(S.empty + 8 * slot, par);   // every lane observes the completed phase
@@ -782,14 +792,17 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
         __threadfence_block();
         sts_flag(S.misc + 4, (uint32_t)(s + 1));
       }
+      if (++slot == g.ns) {
+        slot = 0;
+        par ^= 1u;
+      }
     }
   } else if (warp == kHWarp) {
     // ================================================================ h issuer
     if (lane == 0) {
       int ready_ws = -1;
-      for (int i = 0; i < n_runs; ++i) {
-        const int wsr = i / runs_per_slot, stage = S13 + i / g.w2runs, rpos = i % g.w2runs;
-        const int slot = stage % g.ns;
+      int wsr = 0, rr = 0, stage = S13, rpos = 0, slot = S13 % g.ns;   // run i: slot wsr, run
+      for (int i = 0; i < n_runs; ++i) {                              // rr of it; stage, place
         for (uint32_t it = 0; (int)lds_flag(S.misc) <= stage; ++it) {   // the stage is armed
           if (it > kMbarSpin) {
             atomicOr(p.err, kErrTimeout);
@@ -811,6 +824,15 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
         const uint32_t dst = S.ring + (uint32_t)slot * (uint32_t)g.slot_bytes +
                              (uint32_t)rpos * (uint32_t)g.rb + (uint32_t)g.rw * (ib + is);
         bulk_g2s(dst, p.h + (size_t)wsr * I, 2 * (uint32_t)I, S.full + 8 * slot);
+        if (++rr == runs_per_slot) {
+          rr = 0;
+          ++wsr;
+        }
+        if (++rpos == g.w2runs) {
+          rpos = 0;
+          ++stage;
+          if (++slot == g.ns) slot = 0;
+        }
       }
     }
   } else if (warp == kPubWarp) {
@@ -854,11 +876,17 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
   } else {
     // ================================================================ consumers
     const int e0 = seg_lo + 16 * lane;   // the lane's first element of the segment
-    int s = 0;
+    int s = 0, slot = 0;
+    uint32_t par = 0;
+    auto next_slot = [&]() {
+      if (++slot == g.ns) {
+        slot = 0;
+        par ^= 1u;
+      }
+    };
     // ---- W13: the warp's K-segment of row pair pl of every stage
-    for (; s < S13; ++s) {
-      const int slot = s % g.ns;
-      mb_wait_sleep(S.full + 8 * slot, (s / g.ns) & 1, p.err);
+    for (; s < S13; ++s, next_slot()) {
+      mb_wait_sleep(S.full + 8 * slot, par, p.err);
       const W13Stage t = w13_info(S, g, v, G, s);
       if (pl < t.n) {
         float ag = 0.f, au = 0.f;
@@ -880,13 +908,13 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     // the warp with (rl * nseg2 + q2) mod 16 == warp, the same warp for every slot
     const int q2 = warp % g.nseg2, step = kCW / g.nseg2, t0 = warp / g.nseg2;
     const int e2 = q2 * g.kseg2 + 16 * lane, seg2_hi = min(I, q2 * g.kseg2 + g.kseg2);
-    for (; s < S13 + S2; ++s) {
-      const int slot = s % g.ns;
-      mb_wait_sleep(S.full + 8 * slot, (s / g.ns) & 1, p.err);
-      const int i0 = (s - S13) * g.w2runs, nrh = min(g.w2runs, n_runs - i0);
+    int i0 = 0, rr = 0;   // first run of the stage, and its place within its slot's runs
+    for (; s < S13 + S2; ++s, next_slot()) {
+      mb_wait_sleep(S.full + 8 * slot, par, p.err);
+      const int nrh = min(g.w2runs, n_runs - i0);
       const uint32_t st = S.ring + (uint32_t)slot * (uint32_t)g.slot_bytes;
-      for (int r = 0; r < nrh; ++r) {
-        const int i = i0 + r, rr0 = (i % runs_per_slot) * g.rw, nr = min(g.rw, n2 - rr0);
+      for (int r = 0; r < nrh; ++r, rr = rr + 1 == runs_per_slot ? 0 : rr + 1) {
+        const int rr0 = rr * g.rw, nr = min(g.rw, n2 - rr0);
         const int first = rr0 + ((t0 - rr0) & (step - 1));
         if (first >= rr0 + nr) continue;
         const uint32_t rb = st + (uint32_t)r * (uint32_t)g.rb;
@@ -927,6 +955,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           }
         }
       }
+      i0 += nrh;
       __syncwarp();
       if (lane == 0) mb_arrive(S.empty + 8 * slot);
     }
@@ -991,7 +1020,7 @@ D1Geom d1_geom(int H, int I, int grid) {
   };
   g.off_bar = take(16 * kD1MaxStages, 16);
   g.off_pf = take(8 * 16 * kD1MaxStages, 16);
-  g.off_cand = take(12 * 512, 16);
+  g.off_cand = take(8192 + 8 * 32, 16);
   g.off_misc = take(256, 16);
   g.off_act = take(4 * 160 + 32 * 40, 16);
   g.off_yacc = take(4 * (size_t)g.n2max * g.nseg2, 16);
