@@ -126,6 +126,9 @@ __device__ __forceinline__ bool mb_try(uint32_t a, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Timeout bookkeeping is cold: one out-of-line copy keeps it out of every wait loop's code.
+__device__ __noinline__ void flag_timeout(int* err) { atomicOr(err, kErrTimeout); }
+
 // try_wait that lets the hardware suspend the thread until the phase completes (or about 16 us
 // pass), so a waiting warp takes no issue slots from the warps that are working.
 __device__ __forceinline__ bool mb_try_sleep(uint32_t a, uint32_t parity) {
@@ -142,14 +145,14 @@ __device__ __forceinline__ bool mb_try_sleep(uint32_t a, uint32_t parity) {
 __device__ __forceinline__ bool mb_wait_sleep(uint32_t a, uint32_t parity, int* err) {
   for (uint32_t it = 0; it < (1u << 16); ++it)
     if (mb_try_sleep(a, parity)) return true;
-  atomicOr(err, kErrTimeout);
+  flag_timeout(err);
   return false;
 }
 // Bounded wait for the phase of the given parity; false (and the timeout bit) when it runs out.
 __device__ __forceinline__ bool mb_wait(uint32_t a, uint32_t parity, int* err) {
   for (uint32_t it = 0; it < kMbarSpin; ++it)
     if (mb_try(a, parity)) return true;
-  atomicOr(err, kErrTimeout);
+  flag_timeout(err);
   return false;
 }
 // global -> shared bulk copy, completion counted in bytes on the mbarrier at `mb`
@@ -201,12 +204,12 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
 }
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint64_t ldsu64(uint32_t a) {
   uint64_t v;
-  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a));
   return v;
 }
 // flags shared between warps: strong (relaxed, CTA scope) accesses, so a fence on either side
@@ -372,7 +375,7 @@ __device__ __forceinline__ Sm carve(uint32_t base, const D1Geom& g) {
 struct W13Stage {
   int ws, j0, n;
 };
-__device__ __forceinline__ W13Stage w13_stage(const Sm& S, const D1Geom& g, int v, int G, int s) {
+__device__ __noinline__ W13Stage w13_stage(const Sm& S, const D1Geom& g, int v, int G, int s) {
   W13Stage t;
   t.ws = g.sps == 1 ? s : s / g.sps;
   const int part = s - t.ws * g.sps;
@@ -689,7 +692,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           if (old < S13)
             for (uint32_t it = 0; (int)lds_flag(S.misc + 4) <= old; ++it) {
               if (it > kMbarSpin) {
-                atomicOr(p.err, kErrTimeout);
+                flag_timeout(p.err);
                 break;
               }
               __nanosleep(20);
@@ -799,40 +802,55 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     }
   } else if (warp == kHWarp) {
     // ================================================================ h issuer
-    if (lane == 0) {
-      int ready_ws = -1;
-      int wsr = 0, rr = 0, stage = S13, rpos = 0, slot = S13 % g.ns;   // run i: slot wsr, run
-      for (int i = 0; i < n_runs; ++i) {                              // rr of it; stage, place
+    // lanes poll the slots' completion counters together (lane i: slots i and i + 32), so one
+    // round trip to L2 serves every slot that is still open; lane 0 copies h into the stages
+    uint32_t open_lo = 0, open_hi = 0;   // slots still awaited (bit i / i - 32)
+    if (lane < n_act) open_lo |= 1u << lane;
+    if (lane + 32 < n_act) open_hi |= 1u << lane;
+    open_lo = __ballot_sync(0xffffffffu, open_lo != 0);
+    open_hi = __ballot_sync(0xffffffffu, open_hi != 0);
+    int wsr = 0, rr = 0, stage = S13, rpos = 0, slot = S13 % g.ns;   // run i: slot wsr, run
+    for (int i = 0; i < n_runs; ++i) {                              // rr of it; stage, place
+      if (lane == 0)
         for (uint32_t it = 0; (int)lds_flag(S.misc) <= stage; ++it) {   // the stage is armed
           if (it > kMbarSpin) {
-            atomicOr(p.err, kErrTimeout);
+            flag_timeout(p.err);
             break;
           }
           __nanosleep(32);
         }
-        if (wsr != ready_ws) {   // h of this slot complete across the grid
-          for (uint32_t it = 0; ld_acquire_u32(p.ready + wsr) < (unsigned)I; ++it) {
-            if (it >= p.spin_limit) {
-              atomicOr(p.err, kErrTimeout);
-              break;
-            }
-            __nanosleep(64);
+      __syncwarp();
+      const bool want = wsr < 32 ? (open_lo >> wsr) & 1u : (open_hi >> (wsr - 32)) & 1u;
+      if (want) {   // h of this slot complete across the grid (and of any other open slot)
+        for (uint32_t it = 0;; ++it) {
+          bool lo_ok = true, hi_ok = true;
+          if ((open_lo >> lane) & 1u) lo_ok = ld_acquire_u32(p.ready + lane) >= (unsigned)I;
+          if ((open_hi >> lane) & 1u) hi_ok = ld_acquire_u32(p.ready + 32 + lane) >= (unsigned)I;
+          open_lo &= ~__ballot_sync(0xffffffffu, ((open_lo >> lane) & 1u) && lo_ok);
+          open_hi &= ~__ballot_sync(0xffffffffu, ((open_hi >> lane) & 1u) && hi_ok);
+          const bool still = wsr < 32 ? (open_lo >> wsr) & 1u : (open_hi >> (wsr - 32)) & 1u;
+          if (!still) break;
+          if (it >= p.spin_limit) {
+            if (lane == 0) flag_timeout(p.err);
+            break;
           }
-          ready_ws = wsr;
-          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __nanosleep(64);
         }
+        if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      if (lane == 0) {
         const uint32_t dst = S.ring + (uint32_t)slot * (uint32_t)g.slot_bytes +
                              (uint32_t)rpos * (uint32_t)g.rb + (uint32_t)g.rw * (ib + is);
         bulk_g2s(dst, p.h + (size_t)wsr * I, 2 * (uint32_t)I, S.full + 8 * slot);
-        if (++rr == runs_per_slot) {
-          rr = 0;
-          ++wsr;
-        }
-        if (++rpos == g.w2runs) {
-          rpos = 0;
-          ++stage;
-          if (++slot == g.ns) slot = 0;
-        }
+      }
+      if (++rr == runs_per_slot) {
+        rr = 0;
+        ++wsr;
+      }
+      if (++rpos == g.w2runs) {
+        rpos = 0;
+        ++stage;
+        if (++slot == g.ns) slot = 0;
       }
     }
   } else if (warp == kPubWarp) {
@@ -866,7 +884,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           it = 0;
         } else {
           if (it > kMbarSpin) {
-            atomicOr(p.err, kErrTimeout);
+            flag_timeout(p.err);
             break;
           }
           __nanosleep(32);
@@ -904,10 +922,16 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       __syncwarp();
       if (lane == 0) mb_arrive(S.empty + 8 * slot);
     }
-    // ---- W2 + the weighted sum over the active slots: output row rl of a run is handled by
-    // the warp with (rl * nseg2 + q2) mod 16 == warp, the same warp for every slot
+    // ---- W2 + the weighted sum over the active slots: output row rl (of the CTA's rows) is
+    // handled by the warp with (rl * nseg2 + q2) mod 16 == warp, the same warp for every slot.
+    // The warp's first kRowAcc rows keep per-lane partial sums in registers across all slots and
+    // are reduced once at the end; rows past them (very large H only) are reduced per run.
+    constexpr int kRowAcc = 4;
     const int q2 = warp % g.nseg2, step = kCW / g.nseg2, t0 = warp / g.nseg2;
     const int e2 = q2 * g.kseg2 + 16 * lane, seg2_hi = min(I, q2 * g.kseg2 + g.kseg2);
+    float racc[kRowAcc];
+#pragma unroll
+    for (int m = 0; m < kRowAcc; ++m) racc[m] = 0.f;
     int i0 = 0, rr = 0;   // first run of the stage, and its place within its slot's runs
     for (; s < S13 + S2; ++s, next_slot()) {
       mb_wait_sleep(S.full + 8 * slot, par, p.err);
@@ -932,32 +956,32 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           hr[c][0] = a0.x; hr[c][1] = a0.y; hr[c][2] = a0.z; hr[c][3] = a0.w;
           hr[c][4] = a1.x; hr[c][5] = a1.y; hr[c][6] = a1.z; hr[c][7] = a1.w;
         }
-        for (int rl = first; rl < rr0 + nr; rl += 2 * step) {
-          const int ra = rl - rr0;
-          float aa = 0.f, ab = 0.f;
-          if (rl + step < rr0 + nr) {   // two rows of this warp
-            pair_dot<XC2, CHK>(codes + (uint32_t)ra * ib, codes + (uint32_t)(ra + step) * ib,
-                               scales + (uint32_t)ra * is, scales + (uint32_t)(ra + step) * is,
-                               hr, e2, seg2_hi, aa, ab);
-            const float red = warp_sum2(aa, ab, lane);
-            const uint32_t ya = S.yacc + 4 * (uint32_t)(rl * g.nseg2 + q2);
-            if (lane == 0) stsf(ya, ldsf(ya) + red);
-            if (lane == 16) {
-              const uint32_t yb = S.yacc + 4 * (uint32_t)((rl + step) * g.nseg2 + q2);
-              stsf(yb, ldsf(yb) + red);
-            }
-          } else {
-            row_dot<XC2, CHK>(codes + (uint32_t)ra * ib, scales + (uint32_t)ra * is, hr, e2,
-                              seg2_hi, aa);
-            const float red = warp_sum2(aa, 0.f, lane);
-            const uint32_t ya = S.yacc + 4 * (uint32_t)(rl * g.nseg2 + q2);
-            if (lane == 0) stsf(ya, ldsf(ya) + red);
-          }
+#pragma unroll
+        for (int m = 0; m < kRowAcc; ++m) {   // the warp's row t0 + m * step, if in this run
+          const int rl = t0 + m * step;
+          if (rl >= rr0 && rl < rr0 + nr)
+            row_dot<XC2, CHK>(codes + (uint32_t)(rl - rr0) * ib, scales + (uint32_t)(rl - rr0) * is,
+                              hr, e2, seg2_hi, racc[m]);
+        }
+        for (int rl = max(first, t0 + kRowAcc * step); rl < rr0 + nr; rl += step) {
+          float a = 0.f;
+          row_dot<XC2, CHK>(codes + (uint32_t)(rl - rr0) * ib, scales + (uint32_t)(rl - rr0) * is,
+                            hr, e2, seg2_hi, a);
+          const float red = warp_sum2(a, 0.f, lane);
+          const uint32_t ya = S.yacc + 4 * (uint32_t)(rl * g.nseg2 + q2);
+          if (lane == 0) stsf(ya, ldsf(ya) + red);
         }
       }
       i0 += nrh;
       __syncwarp();
       if (lane == 0) mb_arrive(S.empty + 8 * slot);
+    }
+#pragma unroll
+    for (int m = 0; m < kRowAcc; m += 2) {   // the register rows, two per reduction
+      const int ra = t0 + m * step, rbr = t0 + (m + 1) * step;
+      const float red = warp_sum2(racc[m], racc[m + 1], lane);
+      if (lane == 0 && ra < n2) stsf(S.yacc + 4 * (uint32_t)(ra * g.nseg2 + q2), red);
+      if (lane == 16 && rbr < n2) stsf(S.yacc + 4 * (uint32_t)(rbr * g.nseg2 + q2), red);
     }
     consumer_sync();   // every output partial is in shared memory
     const float os = ldsf(S.scal + 4) * p.inv_hscale;
@@ -1004,11 +1028,19 @@ D1Geom d1_geom(int H, int I, int grid) {
   };
   split(H, g.nseg13, g.kseg13, g.xc13);
   split(I, g.nseg2, g.kseg2, g.xc2);
+  g.n2max = 2 * ((H / 2 + grid - 1) / grid);
+  // W2: split rows into more K-segments while every warp's rows still fit its register
+  // accumulators (4): more, shorter tasks spread a stage's rows evenly over the 16 warps
+  while (g.nseg2 < 16 && g.xc2 > 1 &&
+         (g.n2max * 2 * g.nseg2 + 15) / 16 <= 4) {
+    g.nseg2 *= 2;
+    g.kseg2 = (I + g.nseg2 * 512 - 1) / (g.nseg2 * 512) * 512;
+    g.xc2 = g.kseg2 / 512;
+  }
   if (g.nseg13 > 8 || g.nseg2 > 16) return g;
   g.pps = 16 / g.nseg13;
   const int umax = (I / 2 + grid - 1) / grid;   // largest share (two-pair units) of a slot
   g.sps = std::max(1, (2 * umax + g.pps - 1) / g.pps);
-  g.n2max = 2 * ((H / 2 + grid - 1) / grid);
   if ((size_t)g.n2max * g.nseg2 > 1024) return g;
   // small regions first, the ring takes the rest
   size_t o = 0;
@@ -1046,8 +1078,8 @@ D1Geom d1_geom(int H, int I, int grid) {
   // the x staging (2H bytes) uses the ring before the first stage
   if (2 * H > g.ns * g.slot_bytes) return g;
   const bool full13 = H % (g.nseg13 * 512) == 0, full2 = I % (g.nseg2 * 512) == 0;
-  if (full13 && full2 && g.xc13 == 3 && g.xc2 == 2) g.variant = 1;
-  else if (full13 && full2 && g.xc13 == 4 && g.xc2 == 2) g.variant = 2;
+  if (full13 && full2 && g.xc13 == 3 && g.xc2 == 1) g.variant = 1;
+  else if (full13 && full2 && g.xc13 == 4 && g.xc2 == 1) g.variant = 2;
   else g.variant = 0;
   g.ok = g.smem <= (int)kD1SmemMax;
   return g;
@@ -1079,8 +1111,8 @@ cudaError_t launch_decode1(const uint16_t* x, const int* topk_idx, const float* 
   if (!a.g.ok) return cudaErrorInvalidValue;
 
   using Kern = void (*)(D1Args);
-  Kern kern = a.g.variant == 1 ? k_decode1<3, 2, false>
-            : a.g.variant == 2 ? k_decode1<4, 2, false>
+  Kern kern = a.g.variant == 1 ? k_decode1<3, 1, false>
+            : a.g.variant == 2 ? k_decode1<4, 1, false>
                                : k_decode1<kXc, kXc, true>;
   constexpr int kDevs = 64;
   static std::atomic<unsigned> smem_set[kDevs];   // bit per variant: attribute set
