@@ -9,6 +9,12 @@ passes over the instances, then one of the remaining steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
+The default run times the one-token 288-expert layer as the headline (K steps) and then, in
+the same process and one after the other, the one-token 512-expert layer with its shared
+expert, the 32-token decode batch and the 2048-token prefill, each with its own default step
+count; those land in the line's "configs" object (µs per call, roofline, e2e, CPU oracle).
+--only skips them. --gpus N without torchrun re-launches itself under torchrun with N ranks.
+
 --impl reference times the CPU oracle (the plain float32 reference) on the host cores on a
 bounded sample of the same workload.
 """
@@ -46,6 +52,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--instances", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="time the --workload alone (no companion configs)")
     ap.add_argument("--unrouted", action="store_true",
                     help="one-token decode as ft_moe_route + ft_moe_nvfp4_decode (two launches) "
                          "instead of the routed call; the roofline then times the decode launch")
@@ -79,13 +87,19 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works.
+
+    Started before the warm-up and stopped after the kernel replays, so that even a timed
+    region of a fraction of a second falls inside a run of samples; __enter__ waits (up to
+    5 s) for the first sample. summary() reports the samples taken between mark_start() and
+    mark_end() (the timed region and the replays) when there are any, else all of them."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index, self.proc, self.lines = index, None, []
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
@@ -95,16 +109,26 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
 
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.05)          # one more sample after the last replay
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -112,9 +136,16 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        window = [ln for t, ln in self.lines
+                  if self.t_start is not None and self.t_end is not None
+                  and self.t_start - 0.025 <= t <= self.t_end + 0.025]
+        scope = "timed region and kernel replays"
+        if not window:
+            window = [ln for _, ln in self.lines]
+            scope = "warm-up, timed region and kernel replays"
+        sm, mx, reasons = [], None, set()
+        for ln in window:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -127,7 +158,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": scope}
 
 
 def dist_env():
@@ -151,7 +182,7 @@ def layer_flops(spec, n_pairs: int) -> float:
 
 
 # ------------------------------------------------------------------ our implementation
-def run_ours(args, spec, rank, world, local):
+def run_ours(args, spec, rank, world, local, cpu_seconds=20.0):
     import torch
     from nvfp4_mixture_experts_02_gb300 import ftmoe
     from synth.device import make_device_layer
@@ -160,6 +191,7 @@ def run_ours(args, spec, rank, world, local):
     dev = torch.device("cuda", local)
     n_inst = args.instances or spec.instances
     prefill = spec.prefill
+    t_setup = time.perf_counter()
     layers, exps, shs, wss, idxs, ws_ = [], [], [], [], [], []
     touched, pairs = [], []
     for inst in rank_instances(rank, n_inst):
@@ -198,6 +230,7 @@ def run_ours(args, spec, rank, world, local):
             ftmoe.route(lay.logits, spec.k, idx, w)
         call(lay.x, idx, w, exps[i], shs[i], limit=spec.swiglu_limit, out=outs[i], workspace=ws)
 
+    setup_s = time.perf_counter() - t_setup
     # warm up eagerly (also sets kernel attributes outside capture)
     for i in range(min(n_inst, 3)):
         step(i)
@@ -233,13 +266,14 @@ def run_ours(args, spec, rank, world, local):
     # W warm-up steps in the same rotation, ending on the last instance, so the timed region
     # starts on the instance read longest ago (the rotated inputs are larger than L2)
     n_w = max(0, args.warmup)
-    for j in range(n_w):
-        step((j - n_w) % n_inst)
-    torch.cuda.synchronize()
-    barrier(world)
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        for j in range(n_w):
+            step((j - n_w) % n_inst)
+        torch.cuda.synchronize()
+        barrier(world)
+
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clk.mark_start()
         torch.cuda.synchronize()
         barrier(world)
         ev0.record()
@@ -248,13 +282,20 @@ def run_ours(args, spec, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         step_ms = ev0.elapsed_time(ev1)
-        # decode-only replays: the expert kernels' duration for the roofline
-        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        d0.record()
-        run(g_dec, g_dec_r)
-        d1.record()
-        torch.cuda.synchronize()
-        dec_ms = d0.elapsed_time(d1)
+        # the expert kernel's duration for the roofline: the median over at least 5 timed
+        # replays of a graph of decode launches only (one per instance, cold L2 each time)
+        g_roof, n_roof = (g_dec, n_inst) if g_dec is not None else (g_dec_r, rem_k)
+        reps = max(5, min(31, int(0.25e6 / max(1.0, step_ms * 1e3 / steps_done * n_roof))))
+        rep_ms = []
+        for _ in range(reps):
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            d0.record()
+            g_roof.replay()
+            d1.record()
+            torch.cuda.synchronize()
+            rep_ms.append(d0.elapsed_time(d1))
+        clk.mark_end()
+        dec_ms = statistics.median(rep_ms) / n_roof * steps_done
     assert ftmoe.get_error(ws) == 0
     step_ms = max_over_ranks(step_ms, world)
 
@@ -275,18 +316,17 @@ def run_ours(args, spec, rank, world, local):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
                 "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": traffic,
                 "peak_source": src, "us_per_launch": round(dec_us, 3),
+                "replays": reps, "launches_per_replay": n_roof,
                 "kernel": "ft_moe_nvfp4_prefill (plan, activations, W13 and W2 tcgen05 "
-                          "grouped GEMMs, reduce)",
+                          "grouped GEMMs, reduce; the whole call's time)",
                 "hbm_bound_frac": round((bytes_call / (hbm * 1e9)) / (dec_us * 1e-6), 4)}
     else:
         achieved = bytes_call / (dec_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
-                "kernel": ("k_decode (ft_moe_nvfp4_decode_routed: routing, plan, W13+SwiGLU, "
-                           "W2+weighted sum in one launch)" if fused else
-                           "k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in "
-                           "one launch)"),
-                "us_per_launch": round(dec_us, 3)}
+                "kernel": decode_kernel_name(spec, fused),
+                "us_per_launch": round(dec_us, 3), "replays": reps,
+                "launches_per_replay": n_roof}
     res = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": steps_done, "warmup": max(0, args.warmup), "ms_per_step": step_ms / steps_done,
@@ -307,11 +347,22 @@ def run_ours(args, spec, rank, world, local):
                    statistics.mean(touched)},
         "roofline": roof, "e2e": e2e,
         "gpu_launches": (6 if prefill else 1 if fused else 2) * steps_done,
+        "setup_s": round(setup_s, 1),
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(spec, layers[:2], bytes_call)
+        res["cpu_baseline"] = cpu_baseline(spec, layers[:2], bytes_call, cpu_seconds)
     return res
+
+
+def decode_kernel_name(spec, fused):
+    if fused:
+        return ("k_decode1 (ft_moe_nvfp4_decode_routed, one token: routing, W13+SwiGLU, "
+                "W2+weighted sum in one launch)")
+    if spec.T == 1:
+        return "k_decode1 (ft_moe_nvfp4_decode, one token: W13+SwiGLU, W2+weighted sum)"
+    return ("k_decode (ft_moe_nvfp4_decode: plan, W13+SwiGLU, W2+weighted sum in one "
+            "launch)")
 
 
 def measured_traffic(workload):
@@ -427,16 +478,19 @@ def oracle_call_seconds(spec, lay, tokens=None):
     return time.perf_counter() - t0, len(tokens)
 
 
-def cpu_baseline(spec, layers, bytes_call):
+def cpu_baseline(spec, layers, bytes_call, seconds=20.0):
+    """The oracle timed on the host cores on a bounded sample: whole calls for decode
+    batches of up to 32 tokens, else the first tokens of a call (scaled to the whole call),
+    until 2 calls per instance or `seconds` have been spent (at least one call)."""
     secs, calls = 0.0, 0
-    tokens = None if spec.T <= 32 else np.arange(32)
-    deadline = time.perf_counter() + 20.0
+    tokens = None if spec.T <= 32 else np.arange(8)
+    deadline = time.perf_counter() + seconds
     while calls < 2 * len(layers) and time.perf_counter() < deadline:
         s, ntok = oracle_call_seconds(spec, layers[calls % len(layers)], tokens)
         secs += s * (spec.T / ntok)            # scale a token sample to a whole call
         calls += 1
     per_call = secs / max(calls, 1)
-    return {"value": round(bytes_call / per_call / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+    return {"value": round(bytes_call / per_call / 1e9, 4), "unit": "GB/s", "cores": host_threads(),
             "kind": "oracle", "us_per_call": round(per_call * 1e6, 1),
             "sample": f"{calls} layer calls of instances 0-{len(layers) - 1}"
                       + ("" if tokens is None else f" ({len(tokens)} of {spec.T} tokens, scaled)")
@@ -474,7 +528,7 @@ def run_reference(args, spec, rank, world, local):
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": spec.name, "T": spec.T, "E": spec.E, "k": spec.k,
                        "H": spec.H, "I": spec.I, "shared_expert": spec.shared},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": host_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -499,6 +553,14 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+def host_threads():
+    """Host threads the oracle's numpy/BLAS may use: the CPUs this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
 def rank_instances(rank: int, n_inst: int):
     """Layer instances a rank generates and times: ranks run independent replicas, each on
     its own disjoint set of instances (weak scaling, no collective on the data path)."""
@@ -506,17 +568,49 @@ def rank_instances(rank: int, n_inst: int):
 
 
 DEFAULT_STEPS = {1: 24000, 32: 240, 2048: 40}   # by batch size T
+# timed after the headline in a default run, one after the other (each freed before the next)
+COMPANIONS = ["decode_t1_e512_k10_h4096_i1024_shared", "decode_t32_e512_k10_h4096_i1024_shared",
+              "prefill_t2048_e512_k10_h4096_i1024"]
+COMPANION_KEYS = ("value", "unit", "us_per_call", "tokens_per_s", "steps", "warmup",
+                  "ms_per_step", "roofline", "e2e", "cpu_baseline", "clocks", "gpu_launches",
+                  "config", "setup_s")
+
+
+def default_steps(spec):
+    return DEFAULT_STEPS.get(spec.T, 480)
+
+
+def default_warmup(steps):
+    return max(3, min(steps // 10, 480))
+
+
+def spawn_ranks(n):
+    """--gpus N outside torchrun: run this same command under torchrun with N ranks."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main():
     args = parse()
     from synth import BY_NAME
     spec = BY_NAME[args.workload]
-    if args.steps is None:
-        args.steps = DEFAULT_STEPS.get(spec.T, 480)
-    if args.warmup is None:
-        args.warmup = max(3, min(args.steps // 10, 480))
     rank, world, local = dist_env()
+    if "RANK" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}", file=sys.stderr)
+        sys.exit(2)
+    explicit_steps = args.steps is not None
+    if args.steps is None:
+        args.steps = default_steps(spec)
+    if args.warmup is None:
+        args.warmup = default_warmup(args.steps)
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -526,11 +620,38 @@ def main():
         res = run_reference(args, spec, rank, world, local)
     else:
         res = run_ours(args, spec, rank, world, local)
+        if args.workload == DEFAULT_WORKLOAD and not args.only:
+            res["configs"] = run_companions(args, rank, world, local, explicit_steps)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_companions(args, rank, world, local, explicit_steps):
+    """The other configs, each in turn with its own default steps (at most K when --steps K
+    was given) and warm-up; the previous config's device memory is freed first."""
+    import gc
+    import torch
+    from synth import BY_NAME
+    out = {}
+    for name in COMPANIONS:
+        gc.collect()
+        torch.cuda.empty_cache()
+        spec = BY_NAME[name]
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.instances, a.unrouted = name, None, False
+        a.steps = default_steps(spec)
+        if explicit_steps:
+            a.steps = max(1, min(a.steps, args.steps))
+        a.warmup = default_warmup(a.steps)
+        r = run_ours(a, spec, rank, world, local, cpu_seconds=8.0)
+        out[name] = {k: r[k] for k in COMPANION_KEYS if k in r}
+        del r
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":

@@ -113,8 +113,12 @@ size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_
 size_t ft_moe_decode_smem_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                                 int32_t has_shared);
 
-/* Zero a workspace once after allocating it (the error word and the reduction counters
- * must start at zero; every call leaves them at zero again). Enqueued on `stream`. */
+/* Zero a workspace once after allocating it. Enqueued on `stream`.
+ * Only the first FT_MOE_WORKSPACE_HEAD_BYTES bytes (the error word and the barrier and
+ * completion counters) must be zero before a call, and every call leaves them at zero
+ * again; the rest is scratch that a call writes before it reads it, so its contents
+ * (stale results, NaN bit patterns) never reach an output. */
+#define FT_MOE_WORKSPACE_HEAD_BYTES 1024
 ft_status ft_moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -203,6 +207,17 @@ const char* ft_moe_last_cuda_error(void);
 /* Synchronise `stream`, read the workspace error word, clear it, and return FT_OK or the
  * first error flagged since the last call (FT_ERR_DEVICE_FLAG, FT_ERR_TIMEOUT). */
 ft_status ft_moe_get_error(void* workspace, void* stream);
+
+/* Test hook for the failure path; the pages have no counterpart. Sets, for this process,
+ * how many times a decode kernel polls for the other CTAs' results (the grid barrier of
+ * the several-token kernel, the slot-completion counters of the one-token kernel) before
+ * it gives up: it then sets FT_ERR_TIMEOUT in the workspace error word, goes on with what
+ * it has (the output is then undefined) and returns normally, and the workspace is left
+ * ready for the next call. iterations < 0 restores the default bound (about a second of
+ * waiting); 0 makes a wait give up at its first poll that finds the results incomplete.
+ * Returns FT_OK. Not for production use: set it only while no decode call is being
+ * enqueued by another thread. */
+ft_status ft_moe_debug_set_wait_limit(int64_t iterations);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,16 @@ int sm_count() {
   return n;
 }
 
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+namespace ftmoe {
+
+namespace {
 thread_local cudaError_t t_last_cuda = cudaSuccess;
+std::atomic<long long> g_wait_limit{-1};   // test hook: < 0 means each wait's own default
+}  // namespace
 
 ft_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return FT_OK;
@@ -37,7 +46,10 @@ ft_status cuda_status(cudaError_t e) {
   return FT_ERR_CUDA;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+unsigned wait_limit(unsigned dflt) {
+  const long long v = g_wait_limit.load(std::memory_order_relaxed);
+  return v < 0 ? dflt : (unsigned)v;
+}
 
 ft_status check_experts(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh) {
   if (!ex) return FT_ERR_INVALID_ARG;
@@ -63,6 +75,10 @@ ft_status check_experts(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert
   return FT_OK;
 }
 
+}  // namespace ftmoe
+
+namespace {
+
 ExpertPtrs to_ptrs(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh) {
   ExpertPtrs p;
   p.E = ex->E; p.H = ex->H; p.I = ex->I;
@@ -74,6 +90,10 @@ ExpertPtrs to_ptrs(const ft_nvfp4_experts* ex, const ft_nvfp4_shared_expert* sh)
   p.sh_gate = sh ? sh->gate : nullptr;
   return p;
 }
+
+}  // namespace
+
+namespace ftmoe {
 
 ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx,
                            const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
@@ -92,7 +112,7 @@ ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx
   return FT_OK;
 }
 
-}  // namespace
+}  // namespace ftmoe
 
 extern "C" {
 
@@ -224,6 +244,12 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
 
 const char* ft_moe_last_cuda_error(void) {
   return t_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda);
+}
+
+ft_status ft_moe_debug_set_wait_limit(int64_t iterations) {
+  g_wait_limit.store(iterations < 0 ? -1 : (iterations > 0xffffffffLL ? 0xffffffffLL : iterations),
+                     std::memory_order_relaxed);
+  return FT_OK;
 }
 
 ft_status ft_moe_get_error(void* workspace, void* stream) {

@@ -87,6 +87,7 @@ struct DecodeArgs {
   int upart_units;  // units per CTA slice of upart
   float* part;      // several tokens: W2 result per (pair, output row) [pairs][H]
   int smem_bytes;   // dynamic shared memory granted to each CTA
+  unsigned spin_limit;   // bound of the grid-barrier wait (polls)
 };
 
 // Byte offset of activation element e in a padded row (32 elements per 80 bytes).
@@ -114,11 +115,12 @@ __device__ void grid_arrive(unsigned long long* bar) {
   __syncthreads();
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
 }
-__device__ void grid_wait(unsigned long long* bar, unsigned long long target, int* err) {
+__device__ void grid_wait(unsigned long long* bar, unsigned long long target, int* err,
+                          unsigned limit) {
   if (threadIdx.x == 0) {
     unsigned it = 0;
     while ((long long)(ld_acquire64(bar) - target) < 0) {
-      if (++it > kSpinLimit) {
+      if (it++ >= limit) {
         atomicOr(err, kErrTimeout);
         break;
       }
@@ -1076,7 +1078,7 @@ __global__ void __launch_bounds__(Warps<NT>::value * 32, 1)
   auto arrive = [&]() { grid_arrive(p.bar); };
   auto wait = [&]() {
     ++n_bar;
-    grid_wait(p.bar, bar_base + (unsigned long long)n_bar * gridDim.x, p.err);
+    grid_wait(p.bar, bar_base + (unsigned long long)n_bar * gridDim.x, p.err, p.spin_limit);
   };
 
   const bool has_shared = p.sh_g13 != nullptr;
@@ -1370,7 +1372,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   const float hscale = (float)std::ldexp(1.0, S);
   if (WL.t1)
     return launch_decode1(x, topk_idx, topk_w, k, ex, limit, hscale, out, ws, WL, grid,
-                          1u << 22, stream, logits, topk_idx_out, topk_w_out);
+                          wait_limit(1u << 22), stream, logits, topk_idx_out, topk_w_out);
 
   DecodeArgs a;
   a.x = x; a.T = T; a.k = k; a.E = ex.E; a.H = ex.H; a.I = ex.I;
@@ -1395,6 +1397,7 @@ cudaError_t launch_decode(const uint16_t* x, int T, const int* topk_idx, const f
   // one CTA per SM: the kernel is a cooperative persistent grid
   const size_t smem = SL.total > kDecodeSmem ? SL.total : kDecodeSmem;
   a.smem_bytes = (int)smem;
+  a.spin_limit = wait_limit(kSpinLimit);
   const bool t1 = decode_nt(T) == 1;
   const int vi = t1 ? 0 : 1;
   constexpr int kDevs = 64;

@@ -4,9 +4,27 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "../../include/ft_moe.h"
 #include "ftmoe_layout.h"
 
 namespace ftmoe {
+
+// FT_ERR_CUDA for a failed runtime call, with the error kept for ft_moe_last_cuda_error
+// (FT_OK for cudaSuccess). Every runtime call whose failure an entry point returns goes
+// through it.
+ft_status cuda_status(cudaError_t e);
+
+// The bound of a decode kernel's waits on other CTAs: `dflt` unless the test hook
+// ft_moe_debug_set_wait_limit set one.
+unsigned wait_limit(unsigned dflt);
+
+// Host checks of a layer call's arguments (experts, shared expert, T, k, limit, pointers
+// and their alignment; ws must be non-null and 256-byte aligned when T > 0). Enqueues
+// nothing; FT_OK or the first failure.
+ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                           const float* topk_w, int32_t k, const ft_nvfp4_experts* ex,
+                           const ft_nvfp4_shared_expert* sh, float limit, const uint16_t* out,
+                           const void* ws);
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int* idx, float* w,
                          cudaStream_t stream);

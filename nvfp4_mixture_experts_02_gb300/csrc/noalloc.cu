@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ft_moe.h"
+#include "ftmoe_internal.h"
 #include "ftmoe_layout.h"
 
 namespace {
@@ -42,8 +43,15 @@ extern "C" ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T,
   if (T == 0) return FT_OK;   // empty batch: nothing to read or write
   if (!x || !topk_idx || !topk_w || !out) return FT_ERR_INVALID_ARG;
   if (T > kMaxDecodeT || k > kMaxTopK || ex->E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
+  // every host check of the workspace entry point, before any CUDA call; the scratch array
+  // (256-byte aligned) takes the workspace's place, so a stand-in address is checked
+  ft_status st = check_layer_args(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out,
+                                  reinterpret_cast<const void*>(uintptr_t(256)));
+  if (st != FT_OK) return st;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FT_ERR_CUDA;
+  st = cuda_status(cudaGetDevice(&dev));
+  if (st != FT_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices) return cuda_status(cudaErrorInvalidDevice);
 
   // One-time set-up per device, with that device current: in host code the array's name
   // is only a stand-in, so its device address is fetched here and kept.
@@ -51,17 +59,18 @@ extern "C" ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T,
   int sms = g_sms[dev].load(std::memory_order_acquire);
   if (ptr == nullptr || sms <= 0) {
     void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || a == nullptr)
-      return FT_ERR_CUDA;
+    if ((st = cuda_status(cudaGetSymbolAddress(&a, g_noalloc_scratch))) != FT_OK) return st;
+    if (a == nullptr) return cuda_status(cudaErrorInvalidSymbol);
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return FT_ERR_CUDA;
+    if ((st = cuda_status(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev))) !=
+        FT_OK)
+      return st;
+    if (n <= 0) return cuda_status(cudaErrorInvalidDevice);
     g_sms[dev].store(n, std::memory_order_release);
     g_scratch_addr[dev].store(a, std::memory_order_release);
     ptr = a;
     sms = n;
   }
-
   // The same scratch layout the workspace entry point uses, for this device's grid.
   const DecodeLayout L(T, k, ex->E, ex->H, ex->I, sh != nullptr, sms < kMaxGrid ? sms : kMaxGrid);
   if (L.total > kNoAllocScratchBytes) return FT_ERR_WORKSPACE_TOO_SMALL;   // beyond the array
@@ -70,7 +79,7 @@ extern "C" ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T,
   // counter (the head of the layout, before the activation copy) must start at zero; the
   // rest is written before it is read within a call.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ptr, 0, L.xf, s) != cudaSuccess) return FT_ERR_CUDA;
+  if ((st = cuda_status(cudaMemsetAsync(ptr, 0, L.xf, s))) != FT_OK) return st;
   return ft_moe_nvfp4_decode(x, T, topk_idx, topk_w, k, ex, sh, swiglu_limit, out, ptr,
                              kNoAllocScratchBytes, stream);
 }

@@ -25,7 +25,12 @@ STATUS_NAMES = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_UNSUPPORTED_SHAP
 EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_workspace_bytes",
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
             "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
-            "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes"]
+            "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes",
+            "ft_moe_debug_set_wait_limit"]
+
+# Leading bytes of a workspace that must be zero before a call (FT_MOE_WORKSPACE_HEAD_BYTES);
+# the rest is scratch whose contents never reach an output.
+WORKSPACE_HEAD_BYTES = 1024
 
 
 class FtError(RuntimeError):
@@ -80,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ft_moe_last_cuda_error.restype = ctypes.c_char_p
     lib.ft_moe_get_error.restype = ctypes.c_int
     lib.ft_moe_get_error.argtypes = [vp, vp]
+    lib.ft_moe_debug_set_wait_limit.restype = ctypes.c_int
+    lib.ft_moe_debug_set_wait_limit.argtypes = [ctypes.c_int64]
     return lib
 
 
@@ -275,6 +282,28 @@ def new_workspace(T, k, experts: NvFP4Experts, has_shared, prefill=False, device
     return ws
 
 
+# Calls made without a workspace share one per (device, stream): launches on one stream run
+# in order, so a call never finds its workspace in use by an earlier call that is still
+# running. It grows (a new, larger one) when a call needs more; nothing is allocated on
+# calls that fit.
+_DEFAULT_WS = {}
+
+
+def default_workspace(T, k, experts: NvFP4Experts, has_shared, prefill=False, stream=None):
+    """The workspace a call without one uses: kept per (device, stream) and reused."""
+    n = workspace_bytes(T, k, experts.E, experts.H, experts.I, has_shared, prefill)
+    if n == 0:
+        return new_workspace(T, k, experts, has_shared, prefill, stream=stream)
+    if stream is None:
+        stream = torch.cuda.current_stream(experts.device_index)
+    key = (experts.device_index, stream.cuda_stream)
+    ws = _DEFAULT_WS.get(key)
+    if ws is None or ws.numel() < n:
+        ws = new_workspace(T, k, experts, has_shared, prefill, stream=stream)
+        _DEFAULT_WS[key] = ws
+    return ws
+
+
 def _call_tensors(experts, shared, x, out, workspace, T_name="x"):
     """Checks shared by the layer calls: x [T,H] and out [T,H] (bf16 bits), the shared expert
     against the routed ones, the workspace (1-byte elements: numel() is its size in bytes).
@@ -320,8 +349,8 @@ def decode(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, works
            stream=None):
     """ft_moe_nvfp4_decode: x bf16 [T,H] (T <= 64) -> out bf16 [T,H]."""
     if workspace is None:
-        workspace = new_workspace(x.shape[0], topk_idx.shape[1], experts, shared is not None,
-                                  stream=stream)
+        workspace = default_workspace(x.shape[0], topk_idx.shape[1], experts, shared is not None,
+                                      stream=stream)
     return _layer(_LIB.ft_moe_nvfp4_decode, "ft_moe_nvfp4_decode", x, topk_idx, topk_w,
                   experts, shared, limit, out, workspace, stream)
 
@@ -347,7 +376,7 @@ def decode_routed(x, logits, k, experts, shared=None, limit=7.0, out=None, topk_
     """ft_moe_nvfp4_decode_routed: the layer from the router logits f32 [T,E] (T <= 64); one
     launch for T = 1. topk_idx / topk_w (int32 / f32 [T,k]), when given, receive the slots."""
     if workspace is None:
-        workspace = new_workspace(x.shape[0], k, experts, shared is not None, stream=stream)
+        workspace = default_workspace(x.shape[0], k, experts, shared is not None, stream=stream)
     dev, T, out = _call_tensors(experts, shared, x, out, workspace)
     _need(logits, "logits", dev, _F32, (T, experts.E))
     if topk_idx is not None:
@@ -368,8 +397,8 @@ def prefill(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, work
             stream=None):
     """ft_moe_nvfp4_prefill: x bf16 [T,H] (any T) -> out bf16 [T,H]."""
     if workspace is None:
-        workspace = new_workspace(x.shape[0], topk_idx.shape[1], experts, shared is not None,
-                                  prefill=True, stream=stream)
+        workspace = default_workspace(x.shape[0], topk_idx.shape[1], experts, shared is not None,
+                                      prefill=True, stream=stream)
     return _layer(_LIB.ft_moe_nvfp4_prefill, "ft_moe_nvfp4_prefill", x, topk_idx, topk_w,
                   experts, shared, limit, out, workspace, stream)
 
@@ -377,3 +406,10 @@ def prefill(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, work
 def get_error(workspace, stream=None) -> int:
     dev = _device_of(workspace, "ft_moe_get_error")
     return _LIB.ft_moe_get_error(_ptr(workspace), _stream(stream, dev))
+
+
+def debug_set_wait_limit(iterations: int | None):
+    """Test hook: how often a decode kernel polls for the other CTAs' results before it
+    flags FT_ERR_TIMEOUT and goes on (None: the default bound)."""
+    _check(_LIB.ft_moe_debug_set_wait_limit(-1 if iterations is None else int(iterations)),
+           "ft_moe_debug_set_wait_limit")

@@ -89,14 +89,23 @@ def sigmoid(z):
     return (np.float32(1.0) / (np.float32(1.0) + np.exp(-z))).astype(np.float32)
 
 
+def _expert_job(job):
+    """expert_forward on one job tuple (module level, so a process pool can run it)."""
+    return expert_forward(*job)
+
+
 def moe_layer(x_bits, logits, k: int, experts, shared=None, limit: float = 7.0,
-              tokens=None, fmt: str = "nvfp4"):
+              tokens=None, fmt: str = "nvfp4", map_fn=map):
     """The whole layer for the token rows ``tokens`` (default: all).
 
     ``experts`` is anything with attributes w13, s13, g13, w2, s2, g2 that can be indexed
     by expert id (numpy arrays, or a lazy accessor that fetches one expert at a time); for
     block-FP8 (``fmt="fp8block"``) g13 and g2 are unused and may be None.
     ``shared`` is None or a dict with keys w13 s13 g13 w2 s2 g2 gate.
+    ``map_fn`` evaluates the experts (one job per distinct expert: its token rows and its
+    weights) and returns their outputs in job order; the default is the builtin map, a
+    process pool's imap serves as well. Each kept (token, slot) pair's expert output is
+    weighted and summed into y_t in slot order j = 0, 1, ..., k-1.
     Returns (y float32 [n, H], idx int32 [n, k], w float32 [n, k]).
     """
     x_all = np.asarray(x_bits)
@@ -106,15 +115,22 @@ def moe_layer(x_bits, logits, k: int, experts, shared=None, limit: float = 7.0,
     x = bf16_bits_to_f32(x_all[tokens])             # [n, H]
     idx, w = route(np.asarray(logits)[tokens], k)
     n, H = x.shape
-    y = np.zeros((n, H), dtype=np.float32)
-    for j in range(k):                               # slot order: sum_j w_tj * E_tj(x_t)
-        for e in np.unique(idx[:, j]):
-            rows = np.nonzero(idx[:, j] == e)[0]
+    experts_used = np.unique(idx)
+    where = [np.nonzero(idx == e) for e in experts_used]   # (token rows, slots) per expert
+
+    def jobs():
+        for e, (rows, _) in zip(experts_used, where):
             g13 = None if experts.g13 is None else experts.g13[e]
             g2 = None if experts.g2 is None else experts.g2[e]
-            out = expert_forward(x[rows], experts.w13[e], experts.s13[e], g13,
-                                 experts.w2[e], experts.s2[e], g2, limit, fmt)
-            y[rows] += w[rows, j][:, None] * out
+            yield (x[rows], experts.w13[e], experts.s13[e], g13, experts.w2[e], experts.s2[e],
+                   g2, limit, fmt)
+
+    pair_out = np.zeros((n, k, H), dtype=np.float32)          # E_tj(x_t) per kept pair
+    for (rows, slots), out in zip(where, map_fn(_expert_job, jobs())):
+        pair_out[rows, slots] = out
+    y = np.zeros((n, H), dtype=np.float32)
+    for j in range(k):                               # slot order: sum_j w_tj * E_tj(x_t)
+        y += w[:, j][:, None] * pair_out[:, j]
     if shared is not None:
         gv = bf16_bits_to_f32(shared["gate"])
         s = sigmoid(x @ gv)                           # [n] float32

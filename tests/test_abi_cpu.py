@@ -172,3 +172,28 @@ def test_header_serves_a_plain_c_caller(lib, tmp_path):
     version, status, ws, st = run.stdout.strip().split("|")
     assert int(version) == lib.abi_version() and status.startswith("FT_ERR_MISALIGNED")
     assert int(ws) == lib.workspace_bytes(1, 2, 8, 256, 128, False) and int(st) == 1
+
+
+@pytest.mark.parametrize("call,expect", [
+    (dict(limit=-1.0), 1),                       # SwiGLU limit out of range
+    (dict(x=0x20002), 3),                        # misaligned activations
+    (dict(ex=dict(H=200)), 2),                   # H not a multiple of 128
+    (dict(ex=dict(w13=0)), 1),                   # null weight pointer
+])
+def test_noalloc_checks_every_argument_before_any_cuda_call(lib, call, expect):
+    """ft_moe_nvfp4_decode_noalloc runs all the workspace entry point's host checks before
+    its first CUDA call: with no GPU here, a check that came later would surface as
+    FT_ERR_CUDA instead of the argument's own status."""
+    call = dict(call)
+    ex = _experts(lib, **call.pop("ex", {}))
+    a = dict(x=0x20000, idx=0x30000, w=0x40000, out=0x50000, limit=7.0)
+    a.update(call)
+    st = lib.lib().ft_moe_nvfp4_decode_noalloc(a["x"], 1, a["idx"], a["w"], 2, ctypes.byref(ex),
+                                               None, a["limit"], a["out"], None)
+    assert st == expect, lib.status_string(st)
+
+
+def test_wait_limit_hook(lib):
+    assert lib.lib().ft_moe_debug_set_wait_limit(0) == 0
+    assert lib.lib().ft_moe_debug_set_wait_limit(-1) == 0
+    lib.debug_set_wait_limit(None)

@@ -70,3 +70,28 @@ def test_measured_traffic_is_dropped_when_the_source_changes(tmp_path, monkeypat
     assert bench.measured_traffic("w1") is None
     assert bench.measured_traffic("w2") == 200
 
+
+
+def test_clock_summary_keeps_the_timed_window():
+    clk = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    clk.lines = [(1.0, row.format(sm=1000, cap="Not Active")),      # before: idle clock
+                 (2.0, row.format(sm=2070, cap="Active")),
+                 (2.1, row.format(sm=2060, cap="Not Active")),
+                 (9.0, row.format(sm=800, cap="Not Active"))]        # after
+    clk.t_start, clk.t_end = 1.9, 2.2
+    s = clk.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2065 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "timed region and kernel replays"
+    clk.t_start, clk.t_end = 5.0, 5.1                                # no sample inside
+    s = clk.summary()
+    assert s["samples"] == 4 and s["window"].startswith("warm-up")
+
+
+def test_gpus_must_match_the_launched_world(tmp_path):
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "WORLD_SIZE" in r.stderr

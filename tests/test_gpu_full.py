@@ -11,7 +11,7 @@ from synth import (DECODE_B1_DEEP, DECODE_B1_E288, DECODE_B1_E512, DECODE_B8_E51
                    DECODE_B32_E512, LayerSpec, make_layer)
 from synth.device import HostExperts, make_device_layer, nvfp4_experts
 from synth import philox as px
-from tests.layer_util import assert_close, bf16_to_f64, ftmoe
+from tests.layer_util import assert_close, bf16_to_f64, ftmoe, oracle_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +28,7 @@ def test_device_generator_matches_host_generator():
     np.testing.assert_allclose(g13.cpu().numpy(), host.g13, rtol=1e-6)
 
 
-def _device_parity(spec, tokens=None, instance=0):
+def _device_parity(spec, tokens=None, instance=0, pool=False):
     m = ftmoe()
     lay = make_device_layer(spec, instance)
     ex = m.NvFP4Experts(lay.w13, lay.s13, lay.g13, lay.w2, lay.s2, lay.g2)
@@ -43,10 +43,19 @@ def _device_parity(spec, tokens=None, instance=0):
     if tokens is None:
         tokens = np.arange(spec.T)
     host = HostExperts(lay)
-    ref, ref_idx, _ = om.moe_layer(lay.x_bits, lay.logits_np, spec.k, host,
-                                   shared=host.shared_host(), tokens=tokens)
-    assert np.array_equal(idx.cpu().numpy()[tokens], ref_idx)
+    with (oracle_pool() if pool else _builtin_map()) as map_fn:
+        ref, ref_idx, _ = om.moe_layer(lay.x_bits, lay.logits_np, spec.k, host,
+                                       shared=host.shared_host(), tokens=tokens, map_fn=map_fn)
+    assert np.array_equal(idx.cpu().numpy()[tokens], ref_idx)   # every row, bit-exact
     return assert_close(bf16_to_f64(y)[tokens], ref, spec.name)
+
+
+class _builtin_map:
+    def __enter__(self):
+        return map
+
+    def __exit__(self, *a):
+        return False
 
 
 def test_full_decode_t1_e288():
@@ -61,8 +70,10 @@ def test_full_decode_t1_e512_shared_other_instance():
     _device_parity(DECODE_B1_E512, instance=47)
 
 
-def test_full_decode_t32_e512_shared_sampled():
-    _device_parity(DECODE_B32_E512, tokens=np.array([0, 9, 17, 31]))
+def test_full_decode_t32_e512_shared_every_row():
+    """The 32-token batch of the 512-expert layer: all 32 output rows against the oracle,
+    the routed indices of every row bit-exact."""
+    _device_parity(DECODE_B32_E512, pool=True)
 
 
 def test_full_decode_t8_e512_shared_sampled():

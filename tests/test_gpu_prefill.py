@@ -6,7 +6,8 @@ import torch
 from oracle import moe as om
 from synth import PREFILL_T2048, LayerSpec, make_layer
 from synth.device import HostExperts, make_device_layer
-from tests.layer_util import assert_close, bf16_tensor, bf16_to_f64, experts_to_device, ftmoe
+from tests.layer_util import (assert_close, bf16_tensor, bf16_to_f64, experts_to_device, ftmoe,
+                              oracle_pool)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,7 +82,10 @@ def test_prefill_bad_ids_flagged():
     assert m.get_error(ws) == 6
 
 
-def test_full_prefill_t2048_sampled():
+def test_full_prefill_t2048_every_row():
+    """The 2048-token prefill of the 512-expert layer: all 2048 output rows against the
+    oracle (experts evaluated on a pool of host processes), the routed indices of every
+    row bit-exact."""
     spec = PREFILL_T2048
     m = ftmoe()
     lay = make_device_layer(spec, 0)
@@ -90,8 +94,8 @@ def test_full_prefill_t2048_sampled():
     ws = m.new_workspace(spec.T, spec.k, ex, False, prefill=True)
     y = m.prefill(lay.x, idx, w, ex, None, workspace=ws)
     assert m.get_error(ws) == 0
-    tokens = np.array([0, 1, 777, 1500, 2047])
     host = HostExperts(lay)
-    ref, ref_idx, _ = om.moe_layer(lay.x_bits, lay.logits_np, spec.k, host, tokens=tokens)
-    assert np.array_equal(idx.cpu().numpy()[tokens], ref_idx)
-    assert_close(bf16_to_f64(y)[tokens], ref, spec.name)
+    with oracle_pool() as map_fn:
+        ref, ref_idx, _ = om.moe_layer(lay.x_bits, lay.logits_np, spec.k, host, map_fn=map_fn)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert_close(bf16_to_f64(y), ref, spec.name)

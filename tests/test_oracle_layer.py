@@ -211,3 +211,15 @@ def test_clamp_fires_with_scaled_activations():
     gu = x @ W13.T
     frac = np.mean(np.abs(gu) > 7.0)
     assert frac > 0.1
+
+
+def test_pool_map_gives_the_same_layer():
+    """The GPU parity tests evaluate the oracle's experts on a pool of spawned host
+    processes: the layer must come out bit-identical to the in-process evaluation."""
+    from tests.layer_util import oracle_pool
+    spec = LayerSpec("pool", seed=24, T=6, E=5, k=2, H=64, I=32, shared=True)
+    lay = make_layer(spec)
+    y1, i1, w1 = om.moe_layer(lay.x, lay.logits, 2, lay, shared=lay.shared)
+    with oracle_pool(2) as map_fn:
+        y2, i2, w2 = om.moe_layer(lay.x, lay.logits, 2, lay, shared=lay.shared, map_fn=map_fn)
+    assert np.array_equal(y1, y2) and np.array_equal(i1, i2) and np.array_equal(w1, w2)

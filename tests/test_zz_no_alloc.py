@@ -10,9 +10,11 @@ passes on its own in a fresh process.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+from oracle import moe as om
 from synth import LayerSpec, make_layer
 from tests.layer_util import assert_close, bf16_tensor, bf16_to_f64, experts_to_device, ftmoe
 
@@ -31,7 +33,11 @@ def test_noalloc_matches_workspace_decode_two_calls_in_a_row():
         ref = m.decode(x, idx, w, ex, sh)
         got = m.decode_noalloc(x, idx, w, ex, sh)
         torch.cuda.synchronize()
-        assert_close(bf16_to_f64(got), bf16_to_f64(ref), spec.name)
+        # the same kernels on the same inputs: the same bits
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), spec.name
+        y, ref_idx, _ = om.moe_layer(layer.x, layer.logits, spec.k, layer, shared=layer.shared)
+        assert np.array_equal(idx.cpu().numpy(), ref_idx)
+        assert_close(bf16_to_f64(got), y, spec.name)
 
 
 def test_noalloc_rejects_a_scratch_beyond_its_array():
@@ -45,3 +51,19 @@ def test_noalloc_rejects_a_scratch_beyond_its_array():
     st = m.lib().ft_moe_nvfp4_decode_noalloc(p, T, p, p, k, ctypes.byref(ex), None, 7.0, p,
                                              None)
     assert st == 4, m.status_string(st)   # FT_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_checks_arguments_before_enqueueing():
+    """An invalid argument (here the SwiGLU limit) is refused on the host with its own
+    status, before the call enqueues anything (the CPU suite checks the same with no GPU,
+    where any CUDA call would fail)."""
+    m = ftmoe()
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    ex = m._Experts(8, 256, 128, p, p, p, p, p, p)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st = m.lib().ft_moe_nvfp4_decode_noalloc(p, 1, p, p, 2, ctypes.byref(ex), None, -1.0, p,
+                                             s.cuda_stream)
+    assert st == 1, m.status_string(st)   # FT_ERR_INVALID_ARG
+    assert s.query()
