@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--instances", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=0,
+                    help="streams the end-to-end steps alternate over (default 2)")
     ap.add_argument("--only", action="store_true",
                     help="time the --workload alone (no companion configs)")
     ap.add_argument("--unrouted", action="store_true",
@@ -386,55 +388,34 @@ def measured_traffic(workload):
 
 
 def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
+    """The same layer calls end to end through the host-buffer entry point
+    (ft_moe_layer_from_host): every step copies its x and logits from pinned host memory,
+    runs the layer and copies the output back to pinned host memory, one C call per step."""
     import torch
     from nvfp4_mixture_experts_02_gb300 import ftmoe
     n = min(len(layers), 48)
-    # one pinned staging buffer per step input: x (bf16 bits) then the logits (fp32), so
-    # each step makes one host-to-device copy (x's bytes are a multiple of 256: the logits
-    # stay aligned)
-    nx, nl = spec.T * spec.H * 2, spec.T * spec.E * 4
-    hin = []
-    for l in layers[:n]:
-        buf = np.empty(nx + nl, np.uint8)
-        buf[:nx] = l.x_bits.view(np.uint8).reshape(-1)
-        buf[nx:] = l.logits_np.view(np.uint8).reshape(-1)
-        hin.append(torch.from_numpy(buf).pin_memory())
-    # two streams, each with its own device buffers and workspace, take alternate steps, so
-    # one step's copies overlap the neighbouring step's kernels; every step still copies its
-    # own inputs in and its output out inside the timed region. One-token decode keeps one
-    # stream: its single-launch calls chain better in order on one stream (measured 40.5
-    # against 43.9 us per call for the 288-expert layer).
-    nb = 1 if (not spec.prefill and spec.T == 1) else 2
+    hx = [torch.from_numpy(l.x_bits.view(np.int16).copy()).view(spec.T, spec.H).pin_memory()
+          for l in layers[:n]]
+    hl = [torch.from_numpy(np.ascontiguousarray(l.logits_np)).pin_memory() for l in layers[:n]]
+    # streams take alternate steps, each with its own device buffers and workspace, so one
+    # step's copies overlap the neighbouring step's kernels
+    nb = max(1, args.e2e_streams or 2)
+    prefill = spec.prefill
     streams = [torch.cuda.Stream(device=dev) for _ in range(nb)]
-    wss = [ws] + [ftmoe.new_workspace(spec.T, spec.k, exps[0], spec.shared, prefill=spec.prefill)
+    wss = [ws] + [ftmoe.new_workspace(spec.T, spec.k, exps[0], spec.shared, prefill=prefill)
                   for _ in range(nb - 1)]
-    dins = [torch.empty(nx + nl, dtype=torch.uint8, device=dev) for _ in range(nb)]
-    dxs = [d[:nx].view(torch.int16).view(spec.T, spec.H).view(torch.bfloat16) for d in dins]
-    dls = [d[nx:].view(torch.float32).view(spec.T, spec.E) for d in dins]
-    outs = [torch.empty((spec.T, spec.H), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    mk = lambda shape, dt: [torch.empty(shape, dtype=dt, device=dev) for _ in range(nb)]
+    xd, ld, od = (mk((spec.T, spec.H), torch.bfloat16), mk((spec.T, spec.E), torch.float32),
+                  mk((spec.T, spec.H), torch.bfloat16))
+    idd, wd = mk((spec.T, spec.k), torch.int32), mk((spec.T, spec.k), torch.float32)
     houts = [torch.empty((spec.T, spec.H), dtype=torch.int16).pin_memory() for _ in range(nb)]
-    idxs = [torch.empty((spec.T, spec.k), dtype=torch.int32, device=dev) for _ in range(nb)]
-    wts = [torch.empty((spec.T, spec.k), dtype=torch.float32, device=dev) for _ in range(nb)]
-    call = ftmoe.prefill if spec.prefill else ftmoe.decode
     torch.cuda.synchronize()
 
     def one(i, b):
-        if nb == 1:   # on the current stream: no per-step stream switch on the host
-            _one(i, b)
-            return
-        with torch.cuda.stream(streams[b]):
-            _one(i, b)
-
-    def _one(i, b):
-        dins[b].copy_(hin[i], non_blocking=True)
-        if spec.prefill or getattr(args, "unrouted", False):
-            ftmoe.route(dls[b], spec.k, idxs[b], wts[b])
-            call(dxs[b], idxs[b], wts[b], exps[i], shs[i], limit=spec.swiglu_limit,
-                 out=outs[b], workspace=wss[b])
-        else:   # the routed decode call (one launch for one token)
-            ftmoe.decode_routed(dxs[b], dls[b], spec.k, exps[i], shs[i],
-                                limit=spec.swiglu_limit, out=outs[b], workspace=wss[b])
-        houts[b].copy_(outs[b].view(torch.int16), non_blocking=True)
+        ftmoe.layer_from_host(hx[i], hl[i], spec.k, exps[i], shs[i], limit=spec.swiglu_limit,
+                              out_host=houts[b], x_dev=xd[b], logits_dev=ld[b], out_dev=od[b],
+                              topk_idx_dev=idd[b], topk_w_dev=wd[b], workspace=wss[b],
+                              stream=streams[b])
 
     for i in range(min(n, 4)):
         one(i, i % nb)
@@ -443,14 +424,12 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
-    if nb > 1:
-        for st in streams:
-            st.wait_stream(main)
+    for st in streams:
+        st.wait_stream(main)
     for s_ in range(steps):
         one(s_ % n, s_ % nb)
-    if nb > 1:
-        for st in streams:
-            main.wait_stream(st)
+    for st in streams:
+        main.wait_stream(st)
     e1.record(main)
     torch.cuda.synchronize()
     for w_ in wss:
@@ -459,7 +438,9 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     return {"value": round(bytes_call * steps * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "us_per_call": round(ms * 1e3 / steps, 3),
             "h2d_bytes_per_step": spec.T * spec.H * 2 + spec.T * spec.E * 4,
-            "d2h_bytes_per_step": spec.T * spec.H * 2, "streams": nb}
+            "d2h_bytes_per_step": spec.T * spec.H * 2, "streams": nb,
+            "call": "ft_moe_layer_from_host (pinned host x and logits in, pinned host output "
+                    "out, one C call per step)"}
 
 
 # --------------------------------------------------------------------- CPU oracle arm

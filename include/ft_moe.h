@@ -200,6 +200,33 @@ ft_status ft_moe_nvfp4_decode_noalloc(const uint16_t* x, int32_t T, const int32_
                                       const ft_nvfp4_shared_expert* sh, float swiglu_limit,
                                       uint16_t* out, void* stream);
 
+/*
+ * ft_moe_layer_from_host — the whole layer for T tokens whose activations and router
+ * logits are in host memory, with the output returned to host memory: enqueues on `stream`
+ * the copy of x and of the logits into the caller's device buffers, the layer (for T <= 64
+ * ft_moe_nvfp4_decode_routed; for larger T ft_moe_route into topk_idx_dev / topk_w_dev, then
+ * ft_moe_nvfp4_prefill), and the copy of the output back. Nothing is synchronised: the host
+ * output is complete once `stream` has reached this point. The pages' engine runs the layer
+ * on device-resident activations; this is the same layer with the host transfers of one
+ * call attached, so that one C call serves a caller whose inputs start on the host.
+ *   x_host       bf16 [T, H] in host memory, logits_host float [T, E]; out_host bf16 [T, H]
+ *                (page-locked memory keeps the copies asynchronous; other host memory
+ *                works but makes them synchronous)
+ *   x_dev, logits_dev, out_dev  device buffers of those sizes (16-, 4- and 16-byte aligned)
+ *   topk_idx_dev int32 [T, k], topk_w_dev float [T, k] on the device: required for T > 64
+ *                (they receive the routing slots), optional (NULL) for T <= 64
+ *   workspace    ft_moe_workspace_bytes(T, k, E, H, I, sh != 0, T > 64) bytes, as for the
+ *                call it runs
+ *   Other arguments and errors as for ft_moe_nvfp4_decode_routed / ft_moe_nvfp4_prefill; a
+ *   failed copy returns FT_ERR_CUDA.
+ */
+ft_status ft_moe_layer_from_host(const uint16_t* x_host, const float* logits_host, int32_t T,
+                                 int32_t k, const ft_nvfp4_experts* ex,
+                                 const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                                 uint16_t* out_host, uint16_t* x_dev, float* logits_dev,
+                                 int32_t* topk_idx_dev, float* topk_w_dev, uint16_t* out_dev,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Text of the last CUDA runtime error seen by this thread inside the library (the cause
  * behind an FT_ERR_CUDA); static storage, never NULL. */
 const char* ft_moe_last_cuda_error(void);

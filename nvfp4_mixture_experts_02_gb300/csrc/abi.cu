@@ -242,6 +242,53 @@ ft_status ft_moe_nvfp4_prefill(const uint16_t* x, int32_t T, const int32_t* topk
                                     out, workspace, sms, static_cast<cudaStream_t>(stream)));
 }
 
+ft_status ft_moe_layer_from_host(const uint16_t* x_host, const float* logits_host, int32_t T,
+                                 int32_t k, const ft_nvfp4_experts* ex,
+                                 const ft_nvfp4_shared_expert* sh, float swiglu_limit,
+                                 uint16_t* out_host, uint16_t* x_dev, float* logits_dev,
+                                 int32_t* topk_idx_dev, float* topk_w_dev, uint16_t* out_dev,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  // the layer call's own checks first, on the device buffers, with nothing enqueued
+  ft_status st = check_experts(ex, sh);
+  if (st != FT_OK) return st;
+  if (T < 0 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!(swiglu_limit > 0.0f) || !(swiglu_limit <= 128.0f)) return FT_ERR_INVALID_ARG;
+  if (T == 0) return FT_OK;
+  if (!x_host || !logits_host || !out_host || !x_dev || !logits_dev || !out_dev || !workspace)
+    return FT_ERR_INVALID_ARG;
+  const bool prefill = T > kMaxDecodeT;
+  if (prefill && (!topk_idx_dev || !topk_w_dev)) return FT_ERR_INVALID_ARG;
+  if (!aligned(x_dev, 16) || !aligned(out_dev, 16) || !aligned(logits_dev, 4) ||
+      !aligned(topk_idx_dev, 4) || !aligned(topk_w_dev, 4) || !aligned(workspace, 256))
+    return FT_ERR_MISALIGNED;
+  if (prefill) {
+    if (workspace_bytes < PrefillLayout(T, k, ex->E, ex->H, ex->I, sh != nullptr).total)
+      return FT_ERR_WORKSPACE_TOO_SMALL;
+  } else if (workspace_bytes <
+             DecodeLayout::lower_bound(T, k, ex->E, ex->H, ex->I, sh != nullptr)) {
+    return FT_ERR_WORKSPACE_TOO_SMALL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * ex->H * 2, lb = (size_t)T * ex->E * 4;
+  if ((st = cuda_status(cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s))) != FT_OK)
+    return st;
+  if ((st = cuda_status(cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice,
+                                        s))) != FT_OK)
+    return st;
+  if (prefill) {
+    st = ft_moe_route(logits_dev, T, ex->E, k, topk_idx_dev, topk_w_dev, stream);
+    if (st == FT_OK)
+      st = ft_moe_nvfp4_prefill(x_dev, T, topk_idx_dev, topk_w_dev, k, ex, sh, swiglu_limit,
+                                out_dev, workspace, workspace_bytes, stream);
+  } else {
+    st = ft_moe_nvfp4_decode_routed(x_dev, T, logits_dev, k, ex, sh, swiglu_limit, out_dev,
+                                    topk_idx_dev, topk_w_dev, workspace, workspace_bytes, stream);
+  }
+  if (st != FT_OK) return st;
+  return cuda_status(cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s));
+}
+
 const char* ft_moe_last_cuda_error(void) {
   return t_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda);
 }

@@ -26,7 +26,7 @@ EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_wo
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
             "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
             "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes",
-            "ft_moe_debug_set_wait_limit"]
+            "ft_moe_debug_set_wait_limit", "ft_moe_layer_from_host"]
 
 # Leading bytes of a workspace that must be zero before a call (FT_MOE_WORKSPACE_HEAD_BYTES);
 # the rest is scratch whose contents never reach an output.
@@ -85,6 +85,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ft_moe_last_cuda_error.restype = ctypes.c_char_p
     lib.ft_moe_get_error.restype = ctypes.c_int
     lib.ft_moe_get_error.argtypes = [vp, vp]
+    lib.ft_moe_layer_from_host.restype = ctypes.c_int
+    lib.ft_moe_layer_from_host.argtypes = [vp, vp, i32, i32, ctypes.POINTER(_Experts),
+                                           ctypes.POINTER(_Shared), f32, vp, vp, vp, vp, vp, vp,
+                                           vp, sz, vp]
     lib.ft_moe_debug_set_wait_limit.restype = ctypes.c_int
     lib.ft_moe_debug_set_wait_limit.argtypes = [ctypes.c_int64]
     return lib
@@ -401,6 +405,68 @@ def prefill(x, topk_idx, topk_w, experts, shared=None, limit=7.0, out=None, work
                                       prefill=True, stream=stream)
     return _layer(_LIB.ft_moe_nvfp4_prefill, "ft_moe_nvfp4_prefill", x, topk_idx, topk_w,
                   experts, shared, limit, out, workspace, stream)
+
+
+def _need_host(t, name, dtypes, shape):
+    if t.device.type != "cpu":
+        raise ValueError(f"{name}: expected a host tensor, got one on {t.device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: element type {t.dtype} is not accepted here")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: the tensor must be contiguous")
+    if t.shape != shape:
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def layer_from_host(x_host, logits_host, k, experts, shared=None, limit=7.0, out_host=None,
+                    x_dev=None, logits_dev=None, out_dev=None, topk_idx_dev=None,
+                    topk_w_dev=None, workspace=None, stream=None):
+    """ft_moe_layer_from_host: x bf16 [T,H] and logits f32 [T,E] in host memory (pinned for
+    asynchronous copies) -> out_host bf16 [T,H], with the device buffers given (or made
+    here). Everything is enqueued on the stream; the host output is ready once it is
+    synchronised. Returns out_host."""
+    dev = experts.device_index
+    if x_host.dim() != 2:
+        raise ValueError("x_host: [T, H] expected")
+    T, H, E = x_host.shape[0], experts.H, experts.E
+    _need_host(x_host, "x_host", BF16_BITS, (T, H))
+    _need_host(logits_host, "logits_host", _F32, (T, E))
+    if out_host is None:
+        out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    else:
+        _need_host(out_host, "out_host", BF16_BITS, (T, H))
+    if shared is not None:
+        shared.check_for(experts)
+    cuda = torch.device("cuda", dev)
+    x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=cuda) if x_dev is None else x_dev
+    logits_dev = (torch.empty((T, E), dtype=torch.float32, device=cuda) if logits_dev is None
+                  else logits_dev)
+    out_dev = torch.empty((T, H), dtype=torch.bfloat16, device=cuda) if out_dev is None else out_dev
+    _need(x_dev, "x_dev", dev, BF16_BITS, (T, H))
+    _need(logits_dev, "logits_dev", dev, _F32, (T, E))
+    _need(out_dev, "out_dev", dev, BF16_BITS, (T, H))
+    prefill = T > 64
+    if prefill and topk_idx_dev is None:
+        topk_idx_dev = torch.empty((T, k), dtype=torch.int32, device=cuda)
+    if prefill and topk_w_dev is None:
+        topk_w_dev = torch.empty((T, k), dtype=torch.float32, device=cuda)
+    if topk_idx_dev is not None:
+        _need(topk_idx_dev, "topk_idx_dev", dev, _I32, (T, k))
+    if topk_w_dev is not None:
+        _need(topk_w_dev, "topk_w_dev", dev, _F32, (T, k))
+    if workspace is None:
+        workspace = default_workspace(T, k, experts, shared is not None, prefill=prefill,
+                                      stream=stream)
+    _need(workspace, "workspace", dev, None, None)
+    ex = experts.cstruct()
+    sh = shared.cstruct() if shared is not None else None
+    st = _LIB.ft_moe_layer_from_host(_ptr(x_host), _ptr(logits_host), T, k, ctypes.byref(ex),
+                                     ctypes.byref(sh) if sh is not None else None, float(limit),
+                                     _ptr(out_host), _ptr(x_dev), _ptr(logits_dev),
+                                     _ptr(topk_idx_dev), _ptr(topk_w_dev), _ptr(out_dev),
+                                     _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st, "ft_moe_layer_from_host")
+    return out_host
 
 
 def get_error(workspace, stream=None) -> int:

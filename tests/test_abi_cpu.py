@@ -197,3 +197,26 @@ def test_wait_limit_hook(lib):
     assert lib.lib().ft_moe_debug_set_wait_limit(0) == 0
     assert lib.lib().ft_moe_debug_set_wait_limit(-1) == 0
     lib.debug_set_wait_limit(None)
+
+
+def test_layer_from_host_rejects_invalid_arguments(lib):
+    """Checked on the host before any copy is enqueued (no GPU here: a check that came after
+    a CUDA call would surface as FT_ERR_CUDA)."""
+    f = lib.lib().ft_moe_layer_from_host
+    ex = _experts(lib)
+    good = dict(xh=0x1000, lh=0x2000, T=1, k=2, oh=0x3000, xd=0x20000, ld=0x30000, idd=0,
+                wd=0, od=0x50000, ws=0x60000, wsb=1 << 30, limit=7.0)
+
+    def call(**o):
+        a = dict(good, **o)
+        return f(a["xh"], a["lh"], a["T"], a["k"], ctypes.byref(ex), None, a["limit"], a["oh"],
+                 a["xd"], a["ld"], a["idd"], a["wd"], a["od"], a["ws"], a["wsb"], None)
+
+    assert call(xh=0) == 1                       # null host input
+    assert call(od=0) == 1                       # null device output
+    assert call(limit=0.0) == 1
+    assert call(xd=0x20008) == 3                 # misaligned device activations
+    assert call(ws=0x60010) == 3                 # misaligned workspace
+    assert call(wsb=16) == 4                     # workspace too small
+    assert call(T=100) == 1                      # prefill-sized batch without slot buffers
+    assert call(T=0, xh=0, lh=0, oh=0, xd=0, ld=0, od=0, ws=0) == 0   # empty batch
