@@ -45,18 +45,21 @@ namespace {
 
 constexpr int kPfProducers = 512;        // 16 producer warps: two threads per weight row
 constexpr int kPfThreads = kPfProducers + 32;   // + one warp that issues the MMAs
-constexpr int kPfN = 128;                // max tokens per group (MMA N)
+constexpr int kPfN = 112;                // max tokens per group (MMA N; shared memory sets it)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
 constexpr int kPfStages = 4;              // pipeline stages = chunks in flight per thread
 constexpr int kPfBStages = 8;             // activation tiles in shared memory (2 x kPfStages)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD0 = 0, kColD1 = kPfN, kColA = 2 * kPfN;   // A: 4 stages x 2 x 32 cols
-constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 16 KB per stage
+constexpr uint32_t kColD0 = 0, kColD1 = 128, kColA = 256;   // A: 4 stages x 2 x 32 cols
+constexpr int kBTileBytes = kPfN * kPfKc * 2;                      // 14 KB per stage
 // weight codes: a tile is 4 chunks (128 bytes) of the item's 256 rows, two tensor-map copies
 // (one per 128-row set, 128-byte swizzle) into one of kPfWTiles slots
 constexpr int kPfTileChunks = 4;
 constexpr int kWSetBytes = 128 * 128;
-constexpr int kWTileBytes = 2 * kWSetBytes;                        // 32 KB
+// and, when the scale rows allow a tensor map (K / 16 a multiple of 16 bytes), the 4 chunks'
+// E4M3 scales of the 256 rows (16 bytes a row) after the codes
+constexpr int kSSetBytes = 128 * 16;
+constexpr int kWTileBytes = 2 * kWSetBytes + 2 * kSSetBytes;       // 36 KB
 constexpr int kPfWTiles = 3;
 
 struct PfPlanArgs {
@@ -302,6 +305,9 @@ struct PfGemmArgs {
   int* err;
   // the codes as 2D uint8 tensors [rows][K/2] (routed: all experts' rows; shared expert)
   CUtensorMap tm_w, tm_sh_w;
+  // the scales as 2D uint8 tensors [rows][K/16], when s_tma
+  CUtensorMap tm_s, tm_sh_s;
+  int s_tma;
 };
 
 // 16-byte cp.async to shared memory; src_bytes < 16 zero-fills the rest (0: no read).
@@ -412,6 +418,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     // code tiles of this item: rows of set 0 / set 1 in the tensor map, one tile per 4 chunks
     const int ntiles = (nchunks + kPfTileChunks - 1) / kPfTileChunks;
     const CUtensorMap* tmap = e >= 0 ? &p.tm_w : &p.tm_sh_w;
+    const CUtensorMap* smap = e >= 0 ? &p.tm_s : &p.tm_sh_s;
     const int ybase = e >= 0 ? e * (int)nrows : 0;
     const int y0 = ybase + (kW13 ? rb * 128 : rb * 256);
     const int y1 = ybase + (kW13 ? p.I + rb * 128 : rb * 256 + 128);
@@ -419,9 +426,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       const uint32_t g = ntile + (uint32_t)t;
       const int slot = (int)(g % kPfWTiles);
       const uint32_t dst = sW + (uint32_t)(slot * kWTileBytes);
-      mbar_arrive_tx(&mbar_w[slot], kWTileBytes);
+      mbar_arrive_tx(&mbar_w[slot], p.s_tma ? kWTileBytes : 2 * kWSetBytes);
       tma_load_2d(dst, tmap, t * 128, y0, &mbar_w[slot]);
       tma_load_2d(dst + kWSetBytes, tmap, t * 128, y1, &mbar_w[slot]);
+      if (p.s_tma) {
+        tma_load_2d(dst + 2 * kWSetBytes, smap, t * 16, y0, &mbar_w[slot]);
+        tma_load_2d(dst + 2 * kWSetBytes + kSSetBytes, smap, t * 16, y1, &mbar_w[slot]);
+      }
     };
     if (tid < kPfN) {
       const int n = tid;
@@ -438,21 +449,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     (void)wrow;
     uint32_t sc[kPfStages];
     auto issue = [&](int d, int c) {
-      sc[d] = row_ok ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(srow + (size_t)c * 4) + half)
-                     : 0u;
+      if (!p.s_tma)
+        sc[d] = row_ok ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(srow + (size_t)c * 4) + half)
+                       : 0u;
     };
     // the group's activation tile of chunk c straight into shared-memory stage bst
-    // (cp.async, no registers; padding rows n >= nv are zero-filled): one commit group
+    // (cp.async, no registers; padding rows n >= nv are zero-filled): one commit group. Eight
+    // consecutive threads copy one row's 128 bytes (so a warp's copies are four whole rows),
+    // stored K-major with the 128-byte swizzle: piece j of row n at piece j ^ (n % 8).
     auto issue_b = [&](int c, int bst) {
       const uint32_t bt = smem_addr(sB + bst * kBTileBytes);
 #pragma unroll
-      for (int r = 0; r < kPfN * 8 / kPfProducers; ++r) {
+      for (int r = 0; r < (kPfN * 8 + kPfProducers - 1) / kPfProducers; ++r) {
         const int i = tid + r * kPfProducers;
         if (i < npad * 8) {
-          const int n = (i & 7) + 8 * (i >> 6), j = (i >> 3) & 7;
+          const int n = i >> 3, j = i & 7;
           const bool v = n < nv;
           const size_t src_row = v ? (kW13 ? (size_t)s_tok[n] : (size_t)(p0 + n)) : 0;
-          cp_async16_zfill(bt + btile_off(n, j),
+          cp_async16_zfill(bt + (uint32_t)(n * 128 + ((j ^ (n & 7)) << 4)),
                            p.b_src + src_row * K + (size_t)c * kPfKc + 8 * j, v ? 16u : 0u);
         }
       }
@@ -485,7 +499,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
             for (int ks = 0; ks < kPfKc / 16; ++ks)
               mma_ts_warp(tbase + (s == 0 ? kColD0 : kColD1),
                           tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
-                          smem_desc(b0 + ks * 256, 128, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+                          smem_desc_sw128(b0 + ks * 32, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
           mma_commit_warp(&mbar_done[st]);
         }
         __syncwarp();
@@ -514,6 +528,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
       ok = ok && mbar_wait(&mbar_w[g % kPfWTiles], (g / kPfWTiles) & 1, p.err, kErrTimeout);
       const uint32_t rbase = sW + (uint32_t)((g % kPfWTiles) * kWTileBytes + set * kWSetBytes + m * 128);
       const uint32_t sw = (uint32_t)(m & 7);
+      if (p.s_tma) {   // the row's 16 scale bytes of the tile: chunk d, half h at 4 d + 2 h
+        const uint4 sv = lds_v4(sW + (uint32_t)((g % kPfWTiles) * kWTileBytes + 2 * kWSetBytes +
+                                                set * kSSetBytes + m * 16));
+        const uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int d = 0; d < kPfStages; ++d) sc[d] = (w4[d] >> (16 * half)) & 0xFFFFu;
+      }
 #pragma unroll
       for (int d = 0; d < kPfStages; ++d) {
         const int c = c0 + d;
@@ -669,6 +690,10 @@ PrefillLayout::PrefillLayout(int T, int k, int E, int H, int I, bool shared) {
   total = o;
 }
 
+// 2D uint8 tensor map over the E4M3 scale rows (`row_bytes` = K / 16, a multiple of 16):
+// boxes of 16 bytes (4 chunks) x 128 rows, no swizzle.
+bool scale_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows);
+
 // 2D uint8 tensor map over `rows` rows of `row_bytes` bytes: boxes of 128 bytes x 128 rows,
 // 128-byte swizzle, zero fill past the tensor (rows past an expert read the next expert's,
 // which only ever land in rows whose results are dropped).
@@ -692,6 +717,28 @@ bool code_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool scale_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows) {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = cached.load(std::memory_order_acquire);
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cached.store(encode, std::memory_order_release);
+  }
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {16, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
@@ -759,6 +806,11 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   if (!code_map(&g.tm_w, ex.w13, (uint64_t)ex.H / 2, (uint64_t)ex.E * 2 * ex.I)) return cudaErrorInvalidValue;
   if (shared && !code_map(&g.tm_sh_w, ex.sh_w13, (uint64_t)ex.H / 2, 2 * (uint64_t)ex.I))
     return cudaErrorInvalidValue;
+  g.s_tma = (ex.H / 16) % 16 == 0;
+  if (g.s_tma && !scale_map(&g.tm_s, ex.s13, (uint64_t)ex.H / 16, (uint64_t)ex.E * 2 * ex.I))
+    return cudaErrorInvalidValue;
+  if (g.s_tma && shared && !scale_map(&g.tm_sh_s, ex.sh_s13, (uint64_t)ex.H / 16, 2 * (uint64_t)ex.I))
+    return cudaErrorInvalidValue;
   {
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = pdl_cfg(dim3(num_sms), dim3(kPfThreads), smem_launch, stream, at);
@@ -770,6 +822,11 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   g2.part_out = reinterpret_cast<float*>(base + L.part);
   if (!code_map(&g2.tm_w, ex.w2, (uint64_t)ex.I / 2, (uint64_t)ex.E * ex.H)) return cudaErrorInvalidValue;
   if (shared && !code_map(&g2.tm_sh_w, ex.sh_w2, (uint64_t)ex.I / 2, (uint64_t)ex.H))
+    return cudaErrorInvalidValue;
+  g2.s_tma = (ex.I / 16) % 16 == 0;
+  if (g2.s_tma && !scale_map(&g2.tm_s, ex.s2, (uint64_t)ex.I / 16, (uint64_t)ex.E * ex.H))
+    return cudaErrorInvalidValue;
+  if (g2.s_tma && shared && !scale_map(&g2.tm_sh_s, ex.sh_s2, (uint64_t)ex.I / 16, (uint64_t)ex.H))
     return cudaErrorInvalidValue;
   {
     cudaLaunchAttribute at[1];
