@@ -493,13 +493,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         tc_fence_after();
         {   // the whole warp passes the operands, one elected lane issues
           const uint32_t b0 = smem_addr(sB + (int)(nprod % kPfBStages) * kBTileBytes);
-#pragma unroll
-          for (int s = 0; s < 2; ++s)
-#pragma unroll
-            for (int ks = 0; ks < kPfKc / 16; ++ks)
-              mma_ts_warp(tbase + (s == 0 ? kColD0 : kColD1),
-                          tbase + kColA + (uint32_t)(st * 2 + s) * 32 + ks * 8,
-                          smem_desc_sw128(b0 + ks * 32, 1024), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+          mma8_ts_warp(tbase + kColD0, tbase + kColD1, tbase + kColA + (uint32_t)st * 64,
+                       smem_desc_sw128(b0, 1024), idesc, c > 0 ? 1u : 0u);
           mma_commit_warp(&mbar_done[st]);
         }
         __syncwarp();
