@@ -227,6 +227,54 @@ ft_status ft_moe_layer_from_host(const uint16_t* x_host, const float* logits_hos
                                  int32_t* topk_idx_dev, float* topk_w_dev, uint16_t* out_dev,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Block-FP8 routed experts, the other routed-expert format of the 512-expert model (FreeToken
+ * commit log, 512-expert entry). The pages name the format without defining it; the reading
+ * taken: one E4M3 (fn) byte per weight, one float32 scale per 128 x 128 tile of each weight
+ * matrix (K, the reduction dimension, contiguous), no per-tensor scale, activations bf16.
+ * All device pointers; codes 16-byte aligned, scales 4-byte aligned:
+ *   w13  uint8 [E, 2I, H]   w13_scale float [E, 2I/128, H/128]
+ *   w2   uint8 [E, H, I]    w2_scale  float [E, H/128, I/128]
+ * element value = e4m3(code[r, c]) * scale[r / 128, c / 128]. H and I multiples of 128.
+ */
+typedef struct {
+  int32_t E, H, I;
+  const uint8_t* w13;
+  const float* w13_scale;
+  const uint8_t* w2;
+  const float* w2_scale;
+} ft_fp8block_experts;
+
+/* Optional shared expert in block-FP8 (the same layouts without E) and its gate vector gv
+ * (bf16 [H], 16-byte aligned): y_t += sigmoid(x_t . gv) * shared(x_t). */
+typedef struct {
+  const uint8_t* w13;
+  const float* w13_scale;
+  const uint8_t* w2;
+  const float* w2_scale;
+  const uint16_t* gate;
+} ft_fp8block_shared_expert;
+
+/* Workspace bytes of ft_moe_fp8block_decode for these sizes (0 when they are invalid). */
+size_t ft_moe_fp8block_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                                       int32_t has_shared);
+
+/*
+ * ft_moe_fp8block_decode — the expert part of the layer for a decode batch (0 <= T <= 64)
+ * with block-FP8 experts: y_t = sum_j topk_w[t,j] * W2_e (SwiGLU(W13_e x_t))
+ * [+ sigmoid(x_t . gv) * shared(x_t)], the same layer as ft_moe_nvfp4_decode with the other
+ * weight format. Arguments, routing slots, error flags (an id outside [0, E) or repeated in
+ * a token raises FT_ERR_DEVICE_FLAG and that slot contributes nothing) and the workspace
+ * rule (ft_moe_workspace_init once; calls sharing it ordered on one stream) as for
+ * ft_moe_nvfp4_decode; workspace of ft_moe_fp8block_workspace_bytes bytes. Four kernels
+ * (activations, W13 + SwiGLU, W2, ordered slot sum); deterministic.
+ */
+ft_status ft_moe_fp8block_decode(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                                 const float* topk_w, int32_t k, const ft_fp8block_experts* ex,
+                                 const ft_fp8block_shared_expert* sh, float swiglu_limit,
+                                 uint16_t* out, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
 /* Text of the last CUDA runtime error seen by this thread inside the library (the cause
  * behind an FT_ERR_CUDA); static storage, never NULL. */
 const char* ft_moe_last_cuda_error(void);

@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libftmoe.so")
-SOURCES = ["abi.cu", "route.cu", "decode.cu", "decode1.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "route.cu", "decode.cu", "decode1.cu", "prefill.cu", "noalloc.cu",
+           "fp8block.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

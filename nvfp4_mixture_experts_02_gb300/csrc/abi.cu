@@ -289,6 +289,72 @@ ft_status ft_moe_layer_from_host(const uint16_t* x_host, const float* logits_hos
   return cuda_status(cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s));
 }
 
+}  // extern "C"
+
+namespace {
+
+ft_status check_f8(const ft_fp8block_experts* ex, const ft_fp8block_shared_expert* sh) {
+  if (!ex) return FT_ERR_INVALID_ARG;
+  if (ex->E < 1 || ex->H < 1 || ex->I < 1) return FT_ERR_INVALID_ARG;
+  if (ex->E > kMaxExperts || ex->H % 128 != 0 || ex->I % 128 != 0 || ex->H > 16384 ||
+      ex->I > 8192)
+    return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!ex->w13 || !ex->w13_scale || !ex->w2 || !ex->w2_scale) return FT_ERR_INVALID_ARG;
+  if (!aligned(ex->w13, 16) || !aligned(ex->w2, 16) || !aligned(ex->w13_scale, 4) ||
+      !aligned(ex->w2_scale, 4))
+    return FT_ERR_MISALIGNED;
+  if (sh) {
+    if (!sh->w13 || !sh->w13_scale || !sh->w2 || !sh->w2_scale || !sh->gate)
+      return FT_ERR_INVALID_ARG;
+    if (!aligned(sh->w13, 16) || !aligned(sh->w2, 16) || !aligned(sh->w13_scale, 4) ||
+        !aligned(sh->w2_scale, 4) || !aligned(sh->gate, 16))
+      return FT_ERR_MISALIGNED;
+  }
+  return FT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ft_moe_fp8block_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                                       int32_t has_shared) {
+  if (T < 1 || T > kMaxDecodeT || k < 1 || k > kMaxTopK || E < 1 || k > E || E > kMaxExperts ||
+      H < 128 || I < 128 || H % 128 || I % 128 || H > 16384 || I > 8192)
+    return 0;
+  return F8Layout(T, k, H, I, has_shared != 0).total;
+}
+
+ft_status ft_moe_fp8block_decode(const uint16_t* x, int32_t T, const int32_t* topk_idx,
+                                 const float* topk_w, int32_t k, const ft_fp8block_experts* ex,
+                                 const ft_fp8block_shared_expert* sh, float swiglu_limit,
+                                 uint16_t* out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  ft_status st = check_f8(ex, sh);
+  if (st != FT_OK) return st;
+  if (T < 0 || k < 1 || k > ex->E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!(swiglu_limit > 0.0f) || !(swiglu_limit <= 128.0f)) return FT_ERR_INVALID_ARG;
+  if (T == 0) return FT_OK;
+  if (T > kMaxDecodeT) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !topk_idx || !topk_w || !out || !workspace) return FT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(workspace, 256))
+    return FT_ERR_MISALIGNED;
+  if (workspace_bytes < F8Layout(T, k, ex->H, ex->I, sh != nullptr).total)
+    return FT_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return FT_ERR_CUDA;
+  F8Ptrs p;
+  p.E = ex->E; p.H = ex->H; p.I = ex->I;
+  p.w13 = ex->w13; p.w2 = ex->w2; p.s13 = ex->w13_scale; p.s2 = ex->w2_scale;
+  p.sh_w13 = sh ? sh->w13 : nullptr; p.sh_w2 = sh ? sh->w2 : nullptr;
+  p.sh_s13 = sh ? sh->w13_scale : nullptr; p.sh_s2 = sh ? sh->w2_scale : nullptr;
+  p.sh_gate = sh ? sh->gate : nullptr;
+  return cuda_status(launch_f8_decode(x, T, topk_idx, topk_w, k, p, swiglu_limit, out, workspace,
+                                      sms, static_cast<cudaStream_t>(stream)));
+}
+
 const char* ft_moe_last_cuda_error(void) {
   return t_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda);
 }

@@ -68,4 +68,26 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
                            int k, const ExpertPtrs& ex, float limit, uint16_t* out, void* ws,
                            int num_sms, cudaStream_t stream);
 
+// Block-FP8 routed experts (fp8block.cu): E4M3 codes [rows][K] and float32 scales per
+// 128 x 128 tile [ceil(rows/128)][ceil(K/128)], per expert; the shared expert likewise.
+struct F8Ptrs {
+  int E, H, I;
+  const uint8_t *w13, *w2;
+  const float *s13, *s2;
+  const uint8_t *sh_w13, *sh_w2;   // null without a shared expert
+  const float *sh_s13, *sh_s2;
+  const uint16_t* sh_gate;
+};
+
+// Workspace regions of the block-FP8 decode (byte offsets, 256-byte aligned).
+struct F8Layout {
+  int P = 0;   // (token, slot) pairs, then one pair per token for the shared expert
+  size_t err = 0, xf = 0, xscale = 0, gdot = 0, h = 0, part = 0, total = 0;
+  F8Layout(int T, int k, int H, int I, bool shared);
+};
+
+cudaError_t launch_f8_decode(const uint16_t* x, int T, const int* topk_idx, const float* topk_w,
+                             int k, const F8Ptrs& ex, float limit, uint16_t* out, void* ws,
+                             int num_sms, cudaStream_t stream);
+
 }  // namespace ftmoe

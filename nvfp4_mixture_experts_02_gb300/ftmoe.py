@@ -26,7 +26,8 @@ EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_wo
             "ft_moe_workspace_init", "ft_moe_nvfp4_decode", "ft_moe_nvfp4_prefill",
             "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
             "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes",
-            "ft_moe_debug_set_wait_limit", "ft_moe_layer_from_host"]
+            "ft_moe_debug_set_wait_limit", "ft_moe_layer_from_host",
+            "ft_moe_fp8block_workspace_bytes", "ft_moe_fp8block_decode"]
 
 # Leading bytes of a workspace that must be zero before a call (FT_MOE_WORKSPACE_HEAD_BYTES);
 # the rest is scratch whose contents never reach an output.
@@ -51,6 +52,18 @@ class _Shared(ctypes.Structure):
     _fields_ = [("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
                 ("w13_gscale", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p), ("w2_gscale", ctypes.c_void_p),
+                ("gate", ctypes.c_void_p)]
+
+
+class _F8Experts(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p)]
+
+
+class _F8Shared(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
                 ("gate", ctypes.c_void_p)]
 
 
@@ -89,6 +102,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ft_moe_layer_from_host.argtypes = [vp, vp, i32, i32, ctypes.POINTER(_Experts),
                                            ctypes.POINTER(_Shared), f32, vp, vp, vp, vp, vp, vp,
                                            vp, sz, vp]
+    lib.ft_moe_fp8block_workspace_bytes.restype = sz
+    lib.ft_moe_fp8block_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.ft_moe_fp8block_decode.restype = ctypes.c_int
+    lib.ft_moe_fp8block_decode.argtypes = [vp, i32, vp, vp, i32, ctypes.POINTER(_F8Experts),
+                                           ctypes.POINTER(_F8Shared), f32, vp, vp, sz, vp]
     lib.ft_moe_debug_set_wait_limit.restype = ctypes.c_int
     lib.ft_moe_debug_set_wait_limit.argtypes = [ctypes.c_int64]
     return lib
@@ -236,6 +254,68 @@ class NvFP4Shared:
             raise ValueError("shared expert: H, I and the device must match the routed experts")
 
     def cstruct(self) -> _Shared:
+        return self._cs
+
+
+@dataclass(frozen=True)
+class Fp8BlockExperts:
+    """Block-FP8 routed experts on the device: w13 u8 [E,2I,H] (E4M3 codes), s13 f32
+    [E,2I/128,H/128], w2 u8 [E,H,I], s2 f32 [E,H/128,I/128]. Checked when built."""
+    w13: torch.Tensor
+    s13: torch.Tensor
+    w2: torch.Tensor
+    s2: torch.Tensor
+
+    def __post_init__(self):
+        dev = _device_of(self.w13, "Fp8BlockExperts")
+        if self.w13.dim() != 3 or self.w2.dim() != 3:
+            raise ValueError("Fp8BlockExperts: w13 [E,2I,H] and w2 [E,H,I] are 3-D")
+        E, H, I = self.w13.shape[0], self.w2.shape[1], self.w13.shape[1] // 2
+        t = lambda n: -(-n // 128)
+        _need(self.w13, "w13", dev, None, (E, 2 * I, H))
+        _need(self.s13, "s13", dev, _F32, (E, t(2 * I), t(H)))
+        _need(self.w2, "w2", dev, None, (E, H, I))
+        _need(self.s2, "s2", dev, _F32, (E, t(H), t(I)))
+        object.__setattr__(self, "device_index", dev)
+        object.__setattr__(self, "E", E)
+        object.__setattr__(self, "H", H)
+        object.__setattr__(self, "I", I)
+        object.__setattr__(self, "_cs", _F8Experts(E, H, I, _ptr(self.w13), _ptr(self.s13),
+                                                   _ptr(self.w2), _ptr(self.s2)))
+
+    def cstruct(self) -> _F8Experts:
+        return self._cs
+
+
+@dataclass(frozen=True)
+class Fp8BlockShared:
+    """Block-FP8 shared expert (no E dimension) and its gate vector bf16 [H]."""
+    w13: torch.Tensor
+    s13: torch.Tensor
+    w2: torch.Tensor
+    s2: torch.Tensor
+    gate: torch.Tensor
+
+    def __post_init__(self):
+        dev = _device_of(self.w13, "Fp8BlockShared")
+        H, I = self.w2.shape[0], self.w13.shape[0] // 2
+        t = lambda n: -(-n // 128)
+        _need(self.w13, "shared w13", dev, None, (2 * I, H))
+        _need(self.s13, "shared s13", dev, _F32, (t(2 * I), t(H)))
+        _need(self.w2, "shared w2", dev, None, (H, I))
+        _need(self.s2, "shared s2", dev, _F32, (t(H), t(I)))
+        _need(self.gate, "shared gate", dev, BF16_BITS, (H,))
+        object.__setattr__(self, "device_index", dev)
+        object.__setattr__(self, "H", H)
+        object.__setattr__(self, "I", I)
+        object.__setattr__(self, "_cs", _F8Shared(_ptr(self.w13), _ptr(self.s13), _ptr(self.w2),
+                                                  _ptr(self.s2), _ptr(self.gate)))
+
+    def check_for(self, experts):
+        if (self.device_index, self.H, self.I) != (experts.device_index, experts.H, experts.I):
+            raise ValueError("shared expert: H, I and the device must match the routed experts")
+
+    def cstruct(self) -> _F8Shared:
         return self._cs
 
 
@@ -467,6 +547,40 @@ def layer_from_host(x_host, logits_host, k, experts, shared=None, limit=7.0, out
                                      _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st, "ft_moe_layer_from_host")
     return out_host
+
+
+def fp8block_workspace_bytes(T, k, E, H, I, has_shared) -> int:
+    return _LIB.ft_moe_fp8block_workspace_bytes(T, k, E, H, I, int(bool(has_shared)))
+
+
+def new_fp8block_workspace(T, k, experts: Fp8BlockExperts, has_shared, stream=None):
+    n = fp8block_workspace_bytes(T, k, experts.E, experts.H, experts.I, has_shared)
+    if n == 0:
+        raise FtError(2, "ft_moe_fp8block_workspace_bytes")
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=experts.w13.device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    _check(_LIB.ft_moe_workspace_init(_ptr(ws), n, _stream(stream)), "ft_moe_workspace_init")
+    return ws
+
+
+def fp8block_decode(x, topk_idx, topk_w, experts: Fp8BlockExperts, shared=None, limit=7.0,
+                    out=None, workspace=None, stream=None):
+    """ft_moe_fp8block_decode: x bf16 [T,H] (T <= 64) with block-FP8 experts -> out bf16
+    [T,H]."""
+    if workspace is None:
+        workspace = new_fp8block_workspace(x.shape[0], topk_idx.shape[1], experts,
+                                           shared is not None, stream=stream)
+    dev, T, out = _call_tensors(experts, shared, x, out, workspace)
+    k = _slots(topk_idx, topk_w, T, dev)
+    ex = experts.cstruct()
+    sh = shared.cstruct() if shared is not None else None
+    st = _LIB.ft_moe_fp8block_decode(_ptr(x), T, _ptr(topk_idx), _ptr(topk_w), k,
+                                     ctypes.byref(ex), ctypes.byref(sh) if sh is not None else None,
+                                     float(limit), _ptr(out), _ptr(workspace), workspace.numel(),
+                                     _stream(stream, dev))
+    _check(st, "ft_moe_fp8block_decode")
+    return out
 
 
 def get_error(workspace, stream=None) -> int:

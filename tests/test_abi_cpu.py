@@ -220,3 +220,24 @@ def test_layer_from_host_rejects_invalid_arguments(lib):
     assert call(wsb=16) == 4                     # workspace too small
     assert call(T=100) == 1                      # prefill-sized batch without slot buffers
     assert call(T=0, xh=0, lh=0, oh=0, xd=0, ld=0, od=0, ws=0) == 0   # empty batch
+
+
+def test_fp8block_argument_checks(lib):
+    """Host checks of the block-FP8 decode entry point (nothing reaches the GPU)."""
+    f = lib.lib()
+    ex = lib._F8Experts(8, 256, 128, 0x10000, 0x20000, 0x30000, 0x40000)
+    call = lambda ex_, T=1, k=2, x=0x50000, limit=7.0, ws=0x60000, wsb=1 << 30: \
+        f.ft_moe_fp8block_decode(x, T, 0x70000, 0x80000, k, ctypes.byref(ex_), None, limit,
+                                 0x90000, ws, wsb, None)
+    assert call(lib._F8Experts(8, 200, 128, 0x10000, 0x20000, 0x30000, 0x40000)) == 2   # H
+    assert call(lib._F8Experts(8, 256, 128, 0, 0x20000, 0x30000, 0x40000)) == 1        # null
+    assert call(lib._F8Experts(8, 256, 128, 0x10008, 0x20000, 0x30000, 0x40000)) == 3  # align
+    assert call(ex, k=9) == 1
+    assert call(ex, T=65) == 2
+    assert call(ex, limit=-1.0) == 1
+    assert call(ex, x=0x50002) == 3
+    assert call(ex, wsb=16) == 4
+    assert call(ex, T=0, x=0) == 0
+    assert f.ft_moe_fp8block_workspace_bytes(1, 2, 8, 256, 128, 0) > 0
+    assert f.ft_moe_fp8block_workspace_bytes(65, 2, 8, 256, 128, 0) == 0
+    assert f.ft_moe_fp8block_workspace_bytes(1, 2, 8, 200, 128, 0) == 0
