@@ -54,6 +54,21 @@ def route(logits: np.ndarray, k: int):
     return idx, w
 
 
+def router_logits(x_bits, w_router_bits, gate_bits=None):
+    """The router's logits l_t = W_router x_t (and, with a shared expert, the gate's dot
+    x_t . gv), from bf16 x [T, H], bf16 router weights [E, H] and a bf16 gate [H]: the values
+    decoded to float32 and multiplied with numpy's float32 matmul (a library primitive).
+    Returns (logits float32 [T, E], gate dots float32 [T] or None).
+    (FreeToken commit log: the "moe router / shared gate" kernels compute these two.)"""
+    x = bf16_bits_to_f32(np.asarray(x_bits))
+    w = bf16_bits_to_f32(np.asarray(w_router_bits))
+    logits = (x @ w.T).astype(np.float32)
+    dots = None
+    if gate_bits is not None:
+        dots = (x @ bf16_bits_to_f32(np.asarray(gate_bits))).astype(np.float32)
+    return logits, dots
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     z = np.asarray(z, dtype=np.float32)
     return (z / (np.float32(1.0) + np.exp(-z))).astype(np.float32)

@@ -223,3 +223,43 @@ def test_pool_map_gives_the_same_layer():
     with oracle_pool(2) as map_fn:
         y2, i2, w2 = om.moe_layer(lay.x, lay.logits, 2, lay, shared=lay.shared, map_fn=map_fn)
     assert np.array_equal(y1, y2) and np.array_equal(i1, i2) and np.array_equal(w1, w2)
+
+
+# ------------------------------------------------------------------------ router logits
+def _bf16_bits(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).bfloat16().view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def test_router_logits_one_hot_picks_rows():
+    """x = e_c (one-hot, exact in bf16) gives column c of W_router: l_t[e] = W[e, c]."""
+    rng = np.random.default_rng(5)
+    W = _bf16_bits(rng.standard_normal((6, 32)))
+    x = np.zeros((3, 32), np.float32)
+    cols = [0, 17, 31]
+    for t, c in enumerate(cols):
+        x[t, c] = 1.0
+    lg, _ = om.router_logits(_bf16_bits(x), W)
+    Wf = om.bf16_bits_to_f32(W)
+    for t, c in enumerate(cols):
+        assert np.array_equal(lg[t], Wf[:, c])
+
+
+def test_router_logits_brute_force_fp64():
+    """Every logit and gate dot against a plain fp64 double loop (inputs from bf16 bits)."""
+    rng = np.random.default_rng(6)
+    x = _bf16_bits(rng.standard_normal((4, 48)))
+    W = _bf16_bits(0.05 * rng.standard_normal((5, 48)))
+    g = _bf16_bits(0.05 * rng.standard_normal(48))
+    lg, dots = om.router_logits(x, W, g)
+    xf = om.bf16_bits_to_f32(x).astype(np.float64)
+    Wf = om.bf16_bits_to_f32(W).astype(np.float64)
+    gf = om.bf16_bits_to_f32(g).astype(np.float64)
+    for t in range(4):
+        for e in range(5):
+            ref = sum(xf[t, c] * Wf[e, c] for c in range(48))
+            assert abs(lg[t, e] - ref) <= 1e-5 * (np.abs(xf[t]) @ np.abs(Wf[e])) + 1e-30
+        refd = sum(xf[t, c] * gf[c] for c in range(48))
+        assert abs(dots[t] - refd) <= 1e-5 * (np.abs(xf[t]) @ np.abs(gf)) + 1e-30
+    # a plausible mistake (W not transposed, or x and W swapped) changes the shape or values
+    assert lg.shape == (4, 5)
