@@ -100,6 +100,31 @@ const char* ft_status_string(ft_status s);
 ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                        int32_t* topk_idx, float* topk_w, void* stream);
 
+/*
+ * ft_moe_router_logits — the router's logits l_t = W_router x_t, and the shared expert's gate
+ * dot x_t . gv in the same pass (the FreeToken commit log lists "moe router / shared gate"
+ * kernels beside the MoE GEMV; the pages do not define them further: the plain reading is a
+ * bf16 matrix-vector product with float32 accumulation).
+ *   x         bf16 [T, H], w_router bf16 [E, H], gate bf16 [H] or NULL (16-byte aligned)
+ *   logits    float [T, E] (4-byte aligned), fully overwritten
+ *   gate_dot  float [T], written when gate is given (may be NULL otherwise)
+ *   H a multiple of 8; E <= 4096. Products are exact in float32 and every sum runs in a fixed
+ *   order (deterministic). T = 0 is a no-op.
+ */
+ft_status ft_moe_router_logits(const uint16_t* x, int32_t T, int32_t H, const uint16_t* w_router,
+                               int32_t E, const uint16_t* gate, float* logits, float* gate_dot,
+                               void* stream);
+
+/*
+ * ft_moe_router_route — ft_moe_router_logits then ft_moe_route on those logits, enqueued by
+ * one call (two launches): the routing slots from the activations and the router matrix.
+ * logits [T, E] is the caller's buffer for the intermediate logits; the rest as for the two
+ * calls.
+ */
+ft_status ft_moe_router_route(const uint16_t* x, int32_t T, int32_t H, const uint16_t* w_router,
+                              int32_t E, const uint16_t* gate, int32_t k, float* logits,
+                              float* gate_dot, int32_t* topk_idx, float* topk_w, void* stream);
+
 /* Workspace bytes that decode (prefill = 0) or prefill (prefill = 1) needs for these
  * sizes on the current device; has_shared = 1 when a shared expert is passed. Without a
  * usable device the decode figure is an upper bound for any GPU. Returns 0 for invalid

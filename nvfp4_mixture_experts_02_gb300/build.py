@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libftmoe.so")
 SOURCES = ["abi.cu", "route.cu", "decode.cu", "decode1.cu", "prefill.cu", "noalloc.cu",
-           "fp8block.cu"]
+           "fp8block.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

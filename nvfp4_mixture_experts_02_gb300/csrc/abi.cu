@@ -144,6 +144,35 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                                   static_cast<cudaStream_t>(stream)));
 }
 
+ft_status ft_moe_router_logits(const uint16_t* x, int32_t T, int32_t H, const uint16_t* w_router,
+                               int32_t E, const uint16_t* gate, float* logits, float* gate_dot,
+                               void* stream) {
+  if (T < 0 || H < 8 || H % 8 != 0 || E < 1) return T < 0 || E < 1 ? FT_ERR_INVALID_ARG
+                                                                   : FT_ERR_UNSUPPORTED_SHAPE;
+  if (E > kMaxExperts) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return FT_OK;
+  if (!x || !w_router || !logits || (gate && !gate_dot)) return FT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(gate, 16) || !aligned(logits, 4) ||
+      !aligned(gate_dot, 4))
+    return FT_ERR_MISALIGNED;
+  return cuda_status(launch_router(x, T, H, w_router, E, gate, logits, gate_dot,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+ft_status ft_moe_router_route(const uint16_t* x, int32_t T, int32_t H, const uint16_t* w_router,
+                              int32_t E, const uint16_t* gate, int32_t k, float* logits,
+                              float* gate_dot, int32_t* topk_idx, float* topk_w, void* stream) {
+  // both calls' host checks before anything is enqueued
+  if (T < 0 || E < 1 || k < 1 || k > E) return FT_ERR_INVALID_ARG;
+  if (k > kMaxTopK || E > kMaxExperts || H < 8 || H % 8 != 0) return FT_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return FT_OK;
+  if (!topk_idx || !topk_w) return FT_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(topk_w, 4)) return FT_ERR_MISALIGNED;
+  ft_status st = ft_moe_router_logits(x, T, H, w_router, E, gate, logits, gate_dot, stream);
+  if (st != FT_OK) return st;
+  return ft_moe_route(logits, T, E, k, topk_idx, topk_w, stream);
+}
+
 size_t ft_moe_workspace_bytes(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                               int32_t has_shared, int32_t prefill) {
   if (T < 1 || k < 1 || E < 1 || H < 1 || I < 1 || k > E) return 0;   // T = 0 needs none

@@ -29,6 +29,12 @@ ft_status check_layer_args(const uint16_t* x, int32_t T, const int32_t* topk_idx
 cudaError_t launch_route(const float* logits, int T, int E, int k, int* idx, float* w,
                          cudaStream_t stream);
 
+// Router logits W_router x_t [T][E] and, when gate is not null, the gate dots x_t . gv [T]
+// (router.cu).
+cudaError_t launch_router(const uint16_t* x, int T, int H, const uint16_t* w_router, int E,
+                          const uint16_t* gate, float* logits, float* gate_dot,
+                          cudaStream_t stream);
+
 struct ExpertPtrs {
   int E, H, I;
   const uint8_t *w13, *s13;

@@ -27,7 +27,8 @@ EXPORTED = ["ft_moe_abi_version", "ft_status_string", "ft_moe_route", "ft_moe_wo
             "ft_moe_get_error", "ft_moe_last_cuda_error", "ft_moe_nvfp4_decode_noalloc",
             "ft_moe_nvfp4_decode_routed", "ft_moe_decode_smem_bytes",
             "ft_moe_debug_set_wait_limit", "ft_moe_layer_from_host",
-            "ft_moe_fp8block_workspace_bytes", "ft_moe_fp8block_decode"]
+            "ft_moe_fp8block_workspace_bytes", "ft_moe_fp8block_decode",
+            "ft_moe_router_logits", "ft_moe_router_route"]
 
 # Leading bytes of a workspace that must be zero before a call (FT_MOE_WORKSPACE_HEAD_BYTES);
 # the rest is scratch whose contents never reach an output.
@@ -102,6 +103,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ft_moe_layer_from_host.argtypes = [vp, vp, i32, i32, ctypes.POINTER(_Experts),
                                            ctypes.POINTER(_Shared), f32, vp, vp, vp, vp, vp, vp,
                                            vp, sz, vp]
+    lib.ft_moe_router_logits.restype = ctypes.c_int
+    lib.ft_moe_router_logits.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
+    lib.ft_moe_router_route.restype = ctypes.c_int
+    lib.ft_moe_router_route.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp]
     lib.ft_moe_fp8block_workspace_bytes.restype = sz
     lib.ft_moe_fp8block_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.ft_moe_fp8block_decode.restype = ctypes.c_int
@@ -346,6 +351,51 @@ def route(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, stream=None)
                            _stream(stream, dev))
     _check(st, "ft_moe_route")
     return topk_idx, topk_w
+
+
+def router_logits(x, w_router, gate=None, logits=None, gate_dot=None, stream=None):
+    """ft_moe_router_logits: bf16 x [T,H] and router weights [E,H] (and a bf16 gate [H]) ->
+    (logits f32 [T,E], gate dots f32 [T] or None)."""
+    dev = _device_of(x, "ft_moe_router_logits")
+    if x.dim() != 2 or w_router.dim() != 2:
+        raise ValueError("x [T, H] and w_router [E, H] expected")
+    T, H = x.shape
+    E = w_router.shape[0]
+    _need(x, "x", dev, BF16_BITS, (T, H))
+    _need(w_router, "w_router", dev, BF16_BITS, (E, H))
+    if gate is not None:
+        _need(gate, "gate", dev, BF16_BITS, (H,))
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _need(logits, "logits", dev, _F32, (T, E))
+    if gate is not None and gate_dot is None:
+        gate_dot = torch.empty((T,), dtype=torch.float32, device=x.device)
+    if gate_dot is not None:
+        _need(gate_dot, "gate_dot", dev, _F32, (T,))
+    st = _LIB.ft_moe_router_logits(_ptr(x), T, H, _ptr(w_router), E, _ptr(gate), _ptr(logits),
+                                   _ptr(gate_dot), _stream(stream, dev))
+    _check(st, "ft_moe_router_logits")
+    return logits, gate_dot
+
+
+def router_route(x, w_router, k, gate=None, stream=None):
+    """ft_moe_router_route: the routing slots (idx int32 [T,k], w f32 [T,k]) from x and the
+    router matrix; returns (idx, w, logits, gate dots or None)."""
+    dev = _device_of(x, "ft_moe_router_route")
+    T, H = x.shape
+    E = w_router.shape[0]
+    _need(x, "x", dev, BF16_BITS, (T, H))
+    _need(w_router, "w_router", dev, BF16_BITS, (E, H))
+    if gate is not None:
+        _need(gate, "gate", dev, BF16_BITS, (H,))
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    gate_dot = torch.empty((T,), dtype=torch.float32, device=x.device) if gate is not None else None
+    idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    st = _LIB.ft_moe_router_route(_ptr(x), T, H, _ptr(w_router), E, _ptr(gate), k, _ptr(logits),
+                                  _ptr(gate_dot), _ptr(idx), _ptr(w), _stream(stream, dev))
+    _check(st, "ft_moe_router_route")
+    return idx, w, logits, gate_dot
 
 
 def workspace_bytes(T, k, E, H, I, has_shared, prefill=False) -> int:

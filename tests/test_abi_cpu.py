@@ -241,3 +241,17 @@ def test_fp8block_argument_checks(lib):
     assert f.ft_moe_fp8block_workspace_bytes(1, 2, 8, 256, 128, 0) > 0
     assert f.ft_moe_fp8block_workspace_bytes(65, 2, 8, 256, 128, 0) == 0
     assert f.ft_moe_fp8block_workspace_bytes(1, 2, 8, 200, 128, 0) == 0
+
+
+def test_router_argument_checks(lib):
+    f = lib.lib()
+    assert f.ft_moe_router_logits(0x1000, 0, 256, 0x2000, 8, None, 0x3000, None, None) == 0  # T=0
+    assert f.ft_moe_router_logits(0x1000, 1, 250, 0x2000, 8, None, 0x3000, None, None) == 2  # H%8
+    assert f.ft_moe_router_logits(0x1000, 1, 256, 0x2000, 5000, None, 0x3000, None, None) == 2
+    assert f.ft_moe_router_logits(0, 1, 256, 0x2000, 8, None, 0x3000, None, None) == 1
+    assert f.ft_moe_router_logits(0x1008, 1, 256, 0x2000, 8, None, 0x3000, None, None) == 3
+    assert f.ft_moe_router_logits(0x1000, 1, 256, 0x2000, 8, 0x4000, 0x3000, None, None) == 1
+    assert f.ft_moe_router_route(0x1000, 1, 256, 0x2000, 8, None, 9, 0x3000, None, 0x5000,
+                                 0x6000, None) == 1                                   # k > E
+    assert f.ft_moe_router_route(0x1000, 1, 256, 0x2000, 64, None, 33, 0x3000, None, 0x5000,
+                                 0x6000, None) == 2                                   # k > 32
