@@ -244,6 +244,18 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
 }
+// Named barriers between warp 0 (which arrives) and the service warps (which wait): kBarSlots
+// once the slots' experts and weight arrays are in shared memory (the issuer, which arrives
+// with the stage table, the finisher and the publisher wait), kBarWeights once the router
+// weights and the x scale are (the finisher waits).
+constexpr int kBarSlots = 2, kBarSlotsThreads = 4 * 32;
+constexpr int kBarWeights = 3, kBarWeightsThreads = 2 * 32;
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Two per-lane values summed over the warp in a fixed order: lane 0 ends with the sum of a,
 // lane 16 with the sum of b (one shuffle tree for both).
@@ -331,6 +343,8 @@ __device__ __forceinline__ void row_dot(uint32_t ca, uint32_t sa, const uint32_t
 // Shared-memory addresses of the kernel's regions.
 struct Sm {
   uint32_t full, empty;   // [kD1MaxStages] mbarriers each
+  uint32_t xfree;         // mbarrier: every consumer warp has its activations in registers
+  uint32_t x;             // the token's x (bf16), staged in the ring's last bytes
   uint32_t pf;            // [ns][16] float2: (gate, up) partial sums per consumer warp
   uint32_t cand;          // routing: candidates (u64 keys, experts, logits), then the k slots
   uint32_t red;           // [32] float: max |x| per warp, then gate-dot partials
@@ -342,7 +356,7 @@ struct Sm {
   uint32_t yacc;          // [n2max][nseg2] float output partial sums
   uint32_t share;         // [grid + 1] int: first two-pair unit of each W13 share position
   uint32_t sched;         // [kD1TabStages]: int4 (bytes, copies, W13 slot, W13 first pair | n << 16)
-  uint32_t cps;           // [kD1TabStages][8] uint4 copies: dst, src lo, src hi, bytes
+  uint32_t cps;           // [kD1TabStages][8] uint4 copies: dst, source offset, sel, bytes
   uint32_t ring;
   __device__ __forceinline__ uint32_t act_e(int i) const { return act + 4 * i; }
   __device__ __forceinline__ uint32_t act_w(int i) const { return act + 4 * (40 + i); }
@@ -354,6 +368,8 @@ __device__ __forceinline__ Sm carve(uint32_t base, const D1Geom& g) {
   Sm s;
   s.full = base + g.off_bar;
   s.empty = s.full + 8 * kD1MaxStages;
+  s.xfree = s.empty + 8 * kD1MaxStages;
+  s.x = base + g.off_x;
   s.pf = base + g.off_pf;
   s.cand = base + g.off_cand;
   s.red = base + g.off_misc;
@@ -471,17 +487,25 @@ __device__ __forceinline__ void route_local(const Sm& S, unsigned key, float v, 
   }
 }
 
-// Step 2: candidate c (thread c < 16 k) counts the candidates that beat it; the k best take
-// their slots: slot r = (expert, logit) at cand + 8192 + 8 r.
+// Step 2: every candidate counts the candidates that beat it; the k best take their slots:
+// slot r = (expert, logit) at cand + 8192 + 8 r. P consecutive lanes (the most that the 16
+// consumer warps hold for all 16 k candidates, a power of two) share a candidate, each counting
+// every P-th candidate, and add their counts with shuffles.
 __device__ __forceinline__ void route_rank(const Sm& S, int k, int tid) {
   const int nc = kCW * k;
-  if (tid >= nc) return;
-  const uint64_t me = ldsu64(S.cand + 8 * tid);
+  int P = 1;
+  while (P < 32 && 2 * P * nc <= kCW * 32) P *= 2;
+  if ((tid & ~31) >= nc * P) return;   // whole warps past the last candidate
+  const int c = tid / P, part = tid - c * P;
   int rank = 0;
-  for (int c = 0; c < nc; ++c) rank += ldsu64(S.cand + 8 * c) > me;
-  if (rank < k) {
-    sts32(S.cand + 8192 + 8 * rank, lds32(S.cand + 4096 + 4 * tid));
-    sts32(S.cand + 8192 + 8 * rank + 4, lds32(S.cand + 4096 + 2048 + 4 * tid));
+  if (c < nc) {
+    const uint64_t me = ldsu64(S.cand + 8 * c);
+    for (int j = part; j < nc; j += P) rank += ldsu64(S.cand + 8 * j) > me;
+  }
+  for (int o = P / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+  if (c < nc && part == 0 && rank < k) {
+    sts32(S.cand + 8192 + 8 * rank, lds32(S.cand + 4096 + 4 * c));
+    sts32(S.cand + 8192 + 8 * rank + 4, lds32(S.cand + 4096 + 2048 + 4 * c));
   }
 }
 
@@ -506,6 +530,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       mb_init(S.full + 8 * i, 1);
       mb_init(S.empty + 8 * i, kCW);
     }
+    mb_init(S.xfree, kCW);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sts32(S.misc, 0);
     sts32(S.misc + 4, 0);
@@ -552,7 +577,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
         dot = fmaf(lo, __uint_as_float(gw[j] << 16), dot);
         dot = fmaf(hi, __uint_as_float(gw[j] & 0xFFFF0000u), dot);
       }
-      sts128(S.ring + 2 * (uint32_t)c, q);   // x staged in the ring before any weights land
+      sts128(S.x + 2 * (uint32_t)c, q);   // x staged at the ring's end
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -570,31 +595,27 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     }
     consumer_sync();   // (A) x staged, partials and the routing slots in shared memory
 
-    // ---- warp 0: the slots; every warp: its activations, scaled, into registers
+    // ---- warp 0: the slots' experts and weight arrays, released at once to the issuer (and
+    // the finisher), the router weights after that
+    int e_in = -1;
+    float w_in = 0.f, v0 = 0.f;
+    bool ok = false;
     if (warp == 0) {
-      int e_in = -1;
-      float w_in = 0.f;
       if (routed) {
         if (p.E <= 512) {
-          float v0 = 0.f;
           if (lane < k) {
             e_in = ldsi(S.cand + 8192 + 8 * lane);
             v0 = ldsf(S.cand + 8192 + 8 * lane + 4);
           }
-          w_in = route_weights(v0, k, lane);
         } else {
           route_warp_wide(p.logits, p.E, k, lane, e_in, w_in);
         }
         if (lane >= k) e_in = -1;
-        if (v == 0 && lane < k) {
-          if (p.topk_idx_out) p.topk_idx_out[lane] = e_in;
-          if (p.topk_w_out) p.topk_w_out[lane] = w_in;
-        }
       } else if (lane < k) {
         e_in = p.topk_idx[lane];
         w_in = p.topk_w[lane];
       }
-      bool ok = lane < k && e_in >= 0 && e_in < p.E;
+      ok = lane < k && e_in >= 0 && e_in < p.E;
       if (!routed) {   // given slots: an id outside [0, E) or repeated in an earlier slot
         for (int j = 0; j < k; ++j) {
           const int ej = __shfl_sync(0xffffffffu, e_in, j);
@@ -606,7 +627,6 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
         const int ws = s0 + lane;
         const size_t ee = ok ? (size_t)e_in : 0;
         sts32(S.act_e(ws), ok ? (uint32_t)e_in : 0u);
-        stsf(S.act_w(ws), ok ? w_in : 0.f);
         stsu64(S.ptr + 32 * ws + 0, reinterpret_cast<uint64_t>(p.w13 + ee * 2 * I * (H / 2)));
         stsu64(S.ptr + 32 * ws + 8, reinterpret_cast<uint64_t>(p.s13 + ee * 2 * I * (H / 16)));
         stsu64(S.ptr + 32 * ws + 16, reinterpret_cast<uint64_t>(p.w2 + ee * H * (I / 2)));
@@ -614,13 +634,16 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       }
       if (lane == 0 && has_shared) {
         sts32(S.act_e(0), 0xFFFFFFFFu);
-        stsf(S.act_w(0), 0.f);
         stsu64(S.ptr + 0, reinterpret_cast<uint64_t>(p.sh_w13));
         stsu64(S.ptr + 8, reinterpret_cast<uint64_t>(p.sh_s13));
         stsu64(S.ptr + 16, reinterpret_cast<uint64_t>(p.sh_w2));
         stsu64(S.ptr + 24, reinterpret_cast<uint64_t>(p.sh_s2));
       }
+      __syncwarp();
+      bar_arrive(kBarSlots, kBarSlotsThreads);
     }
+    // ---- every consumer warp: its activations, scaled, into registers; the staging area is
+    // then free for the stages
     float a = 0.f;
     for (int w = 0; w < kCW; ++w) a = fmaxf(a, ldsf(S.red + 4 * w));
     int ex = 0;
@@ -635,8 +658,8 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
       const int e0 = seg_lo + 512 * c + 16 * lane;
       uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
       if (c < g.xc13 && e0 < seg_hi) {
-        q0 = lds128(S.ring + 2 * (uint32_t)e0);
-        q1 = lds128(S.ring + 2 * (uint32_t)e0 + 16);
+        q0 = lds128(S.x + 2 * (uint32_t)e0);
+        q1 = lds128(S.x + 2 * (uint32_t)e0 + 16);
       }
       const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
@@ -645,6 +668,19 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
                                              __uint_as_float(w[m] & 0xFFFF0000u) * down);
         xr[c][m] = *reinterpret_cast<const uint32_t*>(&h2);
       }
+    }
+    __syncwarp();
+    if (lane == 0) mb_arrive(S.xfree);
+    if (warp == 0) {   // the router weights (the finisher needs them for its first stage)
+      if (routed && p.E <= 512) w_in = route_weights(v0, k, lane);
+      if (routed && v == 0 && lane < k) {
+        if (p.topk_idx_out) p.topk_idx_out[lane] = e_in;
+        if (p.topk_w_out) p.topk_w_out[lane] = w_in;
+      }
+      if (lane < k) stsf(S.act_w(s0 + lane), ok ? w_in : 0.f);
+      if (lane == 0 && has_shared) stsf(S.act_w(0), 0.f);
+      __syncwarp();
+      bar_arrive(kBarWeights, kBarWeightsThreads);
     }
   }
   if (warp == kIssuerWarp) {
@@ -662,24 +698,19 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           sts128(S.cps + 16 * (8 * st + c),
                  make_uint4(L.cp[c].dst, L.cp[c].off, L.cp[c].sel, L.cp[c].bytes));
     }
+    __syncwarp();
   }
-  __syncthreads();   // (B) the active slots are known, the ring is free for the weights
+  // No block-wide barrier from here on: the issuer starts as soon as warp 0 has the slots'
+  // weight arrays (named barrier kBarSlots, which also releases the table to the finisher and
+  // the publisher), and holds back only the first stages of the ring slots that the staged x
+  // overlaps until every consumer warp has its activations in registers (mbarrier xfree).
 
   const uint32_t hb = (uint32_t)H / 2, hs = (uint32_t)H / 16;
   const uint32_t ib = (uint32_t)I / 2, is = (uint32_t)I / 16;
 
   if (warp == kIssuerWarp) {
     // ================================================================ stage issuer
-    // the laid-out copies get their absolute sources now that the slots' experts are known
-    for (int i = lane; i < 8 * n_tab; i += 32) {
-      const int st = i >> 3, c = i & 7;
-      if (c < (int)lds32(S.sched + 16 * st + 4)) {
-        const uint4 e = lds128(S.cps + 16 * i);
-        const uint64_t a = ldsu64(S.ptr + 8 * e.z) + e.y;
-        sts128(S.cps + 16 * i, make_uint4(e.x, (uint32_t)a, (uint32_t)(a >> 32), e.w));
-      }
-    }
-    __syncwarp();
+    bar_sync(kBarSlots, kBarSlotsThreads);   // the slots' weight arrays are known
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int slot = 0;
@@ -697,14 +728,17 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
               }
               __nanosleep(20);
             }
+        } else if (s == g.xs0) {   // the first slot that the staged x overlaps
+          mb_wait(S.xfree, 0, p.err);
         }
-        if (s < n_tab) {
+        if (s < n_tab) {   // the laid-out copies, their sources resolved through the slots
           const uint4 e = lds128(S.sched + 16 * s);
+          const int ncp = (int)e.y;
           mb_arrive_tx(full, e.x);
-          for (int c = 0; c < (int)e.y; ++c) {
+          for (int c = 0; c < ncp; ++c) {
             const uint4 q = lds128(S.cps + 16 * (8 * s + c));
-            bulk_g2s_hint(q.x, reinterpret_cast<const void*>(((uint64_t)q.z << 32) | q.y), q.w,
-                          full, pol);
+            bulk_g2s_hint(q.x, reinterpret_cast<const uint8_t*>(ldsu64(S.ptr + 8 * q.z)) + q.y,
+                          q.w, full, pol);
           }
         } else {   // past the table: the same layout, computed here
           const StageLayout L = stage_layout(S, g, v, G, s, S13, n2, r0, runs_per_slot, n_runs, H, I);
@@ -729,6 +763,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
   } else if (warp == kFinWarp) {
     // ================================================================ W13 finisher
     // the slots' scales first: W13 tensor scale, h multiplier, W2 reference scale
+    bar_sync(kBarSlots, kBarSlotsThreads);   // the slots' experts (and the stage table)
     {
       float g13v[2] = {0.f, 0.f}, g2v[2] = {0.f, 0.f}, gmax = 0.f, wmax = 1.f;
 #pragma unroll
@@ -739,8 +774,13 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           g13v[h2] = e >= 0 ? __ldg(p.g13 + e) : __ldg(p.sh_g13);
           g2v[h2] = e >= 0 ? __ldg(p.g2 + e) : __ldg(p.sh_g2);
           gmax = fmaxf(gmax, g2v[h2]);
-          if (e >= 0) wmax = fmaxf(wmax, fabsf(ldsf(S.act_w(i))));
         }
+      }
+      bar_sync(kBarWeights, kBarWeightsThreads);   // the router weights and the x scale
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int i = lane + 32 * h2;
+        if (i < n_act && ldsi(S.act_e(i)) >= 0) wmax = fmaxf(wmax, fabsf(ldsf(S.act_w(i))));
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -857,6 +897,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     // ================================================================ publisher
     // the h of every W13 stage the finisher has stored (observed through its count) is made
     // visible GPU-wide by one fence, then counted into the slots' completion counters
+    bar_sync(kBarSlots, kBarSlotsThreads);   // the stage table
     if (lane == 0) {
       int pub = 0;
       for (uint32_t it = 0; pub < S13; ++it) {
@@ -1050,7 +1091,7 @@ D1Geom d1_geom(int H, int I, int grid) {
     o += bytes;
     return (int)at;
   };
-  g.off_bar = take(16 * kD1MaxStages, 16);
+  g.off_bar = take(16 * kD1MaxStages + 16, 16);
   g.off_pf = take(8 * 16 * kD1MaxStages, 16);
   g.off_cand = take(8192 + 8 * 32, 16);
   g.off_misc = take(256, 16);
@@ -1075,8 +1116,11 @@ D1Geom d1_geom(int H, int I, int grid) {
   g.w2runs = std::min(slot / g.rb, 4);   // two copies per run: at most eight per stage
   if (g.w2runs < 1) return g;
   g.smem = g.off_ring + g.ns * g.slot_bytes;
-  // the x staging (2H bytes) uses the ring before the first stage
+  // x (2H bytes) is staged at the end of the ring: the stages of the first slots land while it
+  // is still being read
   if (2 * H > g.ns * g.slot_bytes) return g;
+  g.off_x = g.off_ring + g.ns * g.slot_bytes - 2 * H;
+  g.xs0 = (g.ns * g.slot_bytes - 2 * H) / g.slot_bytes;
   const bool full13 = H % (g.nseg13 * 512) == 0, full2 = I % (g.nseg2 * 512) == 0;
   if (full13 && full2 && g.xc13 == 3 && g.xc2 == 1) g.variant = 1;
   else if (full13 && full2 && g.xc13 == 4 && g.xc2 == 1) g.variant = 2;

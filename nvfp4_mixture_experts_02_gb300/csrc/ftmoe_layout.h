@@ -38,6 +38,7 @@ struct D1Geom {
   int variant = 0;   // kernel instance: chunk counts fixed at compile time, or checked
   int off_bar = 0, off_pf = 0, off_cand = 0, off_misc = 0, off_act = 0, off_yacc = 0,
       off_tab = 0, off_sched = 0, off_ring = 0, smem = 0;
+  int off_x = 0, xs0 = 0;   // x staged at the end of the ring; the first ring slot it overlaps
 };
 D1Geom d1_geom(int H, int I, int grid);
 
