@@ -446,7 +446,7 @@ __device__ __noinline__ StageLayout stage_layout(const Sm& S, const D1Geom& g, i
       const int i = i0 + r, wsr = i / rps, rr0 = (i - wsr * rps) * g.rw;
       const uint32_t nr = (uint32_t)min(g.rw, n2 - rr0), row = (uint32_t)(r0 + rr0);
       const uint32_t rb = st + (uint32_t)r * (uint32_t)g.rb;
-      L.bytes += nr * (ib + is) + 2 * (uint32_t)I;
+      L.bytes += nr * (ib + is);   // the run's h is counted by the h issuer
       L.cp[L.ncp++] = {rb, row * ib, 4 * (uint32_t)wsr + 2, nr * ib};
       L.cp[L.ncp++] = {rb + (uint32_t)g.rw * ib, row * is, 4 * (uint32_t)wsr + 3, nr * is};
     }
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < g.ns; ++i) {
-      mb_init(S.full + 8 * i, 1);
+      mb_init(S.full + 8 * i, 2);   // the stage issuer twice (W13) or once plus the h issuer
       mb_init(S.empty + 8 * i, kCW);
     }
     mb_init(S.xfree, kCW);
@@ -735,6 +735,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
           const uint4 e = lds128(S.sched + 16 * s);
           const int ncp = (int)e.y;
           mb_arrive_tx(full, e.x);
+          if (s < S13) mb_arrive(full);   // a W13 stage has no h: the second arrival
           for (int c = 0; c < ncp; ++c) {
             const uint4 q = lds128(S.cps + 16 * (8 * s + c));
             bulk_g2s_hint(q.x, reinterpret_cast<const uint8_t*>(ldsu64(S.ptr + 8 * q.z)) + q.y,
@@ -743,6 +744,7 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
         } else {   // past the table: the same layout, computed here
           const StageLayout L = stage_layout(S, g, v, G, s, S13, n2, r0, runs_per_slot, n_runs, H, I);
           mb_arrive_tx(full, L.bytes);
+          if (s < S13) mb_arrive(full);
           for (int c = 0; c < L.ncp; ++c)
             bulk_g2s_hint(
                 L.cp[c].dst,
@@ -842,8 +844,11 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     }
   } else if (warp == kHWarp) {
     // ================================================================ h issuer
-    // lanes poll the slots' completion counters together (lane i: slots i and i + 32), so one
-    // round trip to L2 serves every slot that is still open; lane 0 copies h into the stages
+    // A W2 stage's h bytes are this warp's part of the stage: once the stage's ring slot is
+    // free, lane 0 arrives on its full barrier with them (the stage issuer adds the weight
+    // bytes), and copies each run's h in as soon as that slot's h is complete across the grid.
+    // The lanes poll the slots' completion counters together (lane i: slots i and i + 32), so
+    // one round trip to L2 serves every slot that is still open.
     uint32_t open_lo = 0, open_hi = 0;   // slots still awaited (bit i / i - 32)
     if (lane < n_act) open_lo |= 1u << lane;
     if (lane + 32 < n_act) open_hi |= 1u << lane;
@@ -851,14 +856,33 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     open_hi = __ballot_sync(0xffffffffu, open_hi != 0);
     int wsr = 0, rr = 0, stage = S13, rpos = 0, slot = S13 % g.ns;   // run i: slot wsr, run
     for (int i = 0; i < n_runs; ++i) {                              // rr of it; stage, place
-      if (lane == 0)
-        for (uint32_t it = 0; (int)lds_flag(S.misc) <= stage; ++it) {   // the stage is armed
-          if (it > kMbarSpin) {
-            flag_timeout(p.err);
-            break;
+      if (rpos == 0) {   // the stage's slot free: its previous stage released by the consumers
+        int ok = 1;
+        if (lane == 0) {
+          if (stage >= g.ns) {
+            // that previous stage armed first: the slot's empty barrier is then at most one
+            // phase past it, so the parity wait below cannot take an older phase for it
+            for (uint32_t it = 0; (int)lds_flag(S.misc) <= stage - g.ns; ++it) {
+              if (it > kMbarSpin) {
+                flag_timeout(p.err);
+                ok = 0;
+                break;
+              }
+              __nanosleep(32);
+            }
+            if (ok)
+              ok = mb_wait_sleep(S.empty + 8 * slot, ((uint32_t)(stage / g.ns) & 1u) ^ 1u, p.err);
+          } else if (slot >= g.xs0) {
+            ok = mb_wait_sleep(S.xfree, 0, p.err);
           }
-          __nanosleep(32);
+          if (ok)
+            mb_arrive_tx(S.full + 8 * slot,
+                         (uint32_t)min(g.w2runs, n_runs - i) * 2u * (uint32_t)I);
         }
+        // a wait that ran out leaves the barriers alone from here on (the consumers' own
+        // bounded waits then give up): an arrival in the wrong phase could not be undone
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       __syncwarp();
       const bool want = wsr < 32 ? (open_lo >> wsr) & 1u : (open_hi >> (wsr - 32)) & 1u;
       if (want) {   // h of this slot complete across the grid (and of any other open slot)
