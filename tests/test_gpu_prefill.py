@@ -70,16 +70,44 @@ def test_prefill_deterministic():
         assert torch.equal(y2.view(torch.int16), y1.view(torch.int16))
 
 
-def test_prefill_bad_ids_flagged():
-    layer = make_layer(LayerSpec("pbad", seed=60, T=3, E=8, k=2, H=256, I=128))
+@pytest.mark.parametrize("shared", [False, True], ids=["routed_only", "with_shared"])
+def test_prefill_bad_ids_flagged(shared):
+    """Slots with an id outside [0, E) or repeating an earlier slot of the token are flagged
+    and contribute nothing; a token left without any slot gets only the shared expert (or a
+    zero row). The output is the oracle's experts summed over the kept slots."""
+    layer = make_layer(LayerSpec("pbad", seed=60, T=4, E=8, k=2, H=256, I=128, shared=shared))
     m = ftmoe()
-    ex, _ = experts_to_device(layer)
+    ex, sh = experts_to_device(layer)
     x = bf16_tensor(layer.x)
-    idx = torch.tensor([[1, 9], [2, 2], [0, 5]], dtype=torch.int32, device="cuda")
-    w = torch.full((3, 2), 0.5, dtype=torch.float32, device="cuda")
-    ws = m.new_workspace(3, 2, ex, False, prefill=True)
-    m.prefill(x, idx, w, ex, None, workspace=ws)
+    ids = [[1, 9], [2, 2], [0, 5], [9, -1]]
+    ws_ = [[0.7, 0.3], [0.6, 0.4], [0.5, 0.5], [0.9, 0.1]]
+    idx = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    w = torch.tensor(ws_, dtype=torch.float32, device="cuda")
+    ws = m.new_workspace(4, 2, ex, shared, prefill=True)
+    y = bf16_to_f64(m.prefill(x, idx, w, ex, sh, workspace=ws))
     assert m.get_error(ws) == 6
+    xf = om.bf16_bits_to_f32(layer.x)
+    ref = np.zeros((4, 256), dtype=np.float64)
+    for t in range(4):
+        kept = []
+        for j, e in enumerate(ids[t]):
+            if 0 <= e < 8 and e not in ids[t][:j]:
+                kept.append((e, ws_[t][j]))
+        for e, wt in kept:
+            out = om.expert_forward(xf[t:t + 1], layer.w13[e], layer.s13[e], layer.g13[e],
+                                    layer.w2[e], layer.s2[e], layer.g2[e], 7.0)
+            ref[t] += np.float32(wt) * out[0]
+        if shared:
+            sd = layer.shared
+            gv = om.bf16_bits_to_f32(sd["gate"])
+            out = om.expert_forward(xf[t:t + 1], sd["w13"], sd["s13"], sd["g13"], sd["w2"],
+                                    sd["s2"], sd["g2"], 7.0)
+            ref[t] += om.sigmoid(xf[t] @ gv) * out[0]
+    if shared:
+        assert_close(y, ref, "pbad_shared")
+    else:
+        assert_close(y[:3], ref[:3], "pbad")
+        assert np.all(y[3] == 0.0)
 
 
 def test_full_prefill_t2048_every_row():
