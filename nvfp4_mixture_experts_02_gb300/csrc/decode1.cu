@@ -815,7 +815,9 @@ __global__ void __launch_bounds__(kT1Threads, 1) k_decode1(const __grid_constant
     int slot = 0;
     uint32_t par = 0;
     for (int s = 0; s < S13; ++s) {
-      if (lane == 0) mb_wait_sleep(S.empty + 8 * slot, par, p.err);
+      // a spinning wait: the suspended form wakes about 0.35 us later per stage, and this
+      // chain (stage released -> h stored -> published) gates the W2 stages
+      if (lane == 0) mb_wait(S.empty + 8 * slot, par, p.err);
       __syncwarp();
       (void)mb_try(S.empty + 8 * slot, par);   // every lane observes the completed phase
       const W13Stage t = w13_info(S, g, v, G, s);
