@@ -6,13 +6,15 @@
 // cost is the weight stream: every byte of the selected experts is read once. The kernel is
 // built to keep that stream at the HBM rate:
 //
-// * Roles. Each CTA (one per SM) has 16 consumer warps and three service warps. The stage
+// * Roles. Each CTA (one per SM) has 16 consumer warps and four service warps. The stage
 //   issuer moves weight rows into a ring of shared-memory stages with large 1-D bulk copies
 //   (cp.async.bulk: a few per stage, each a contiguous block of whole rows, completion counted
-//   in bytes on the stage's "full" mbarrier); the copies of a stage are issued by one lane
-//   each. The consumers compute from shared memory and release a stage on its "empty"
-//   mbarrier. The finisher turns the consumers' partial sums of a W13 stage into h (clamped
-//   SwiGLU) and publishes it; the h issuer copies h into the W2 stages.
+//   in bytes on the stage's "full" mbarrier, which takes two arrivals: the issuer's with the
+//   weight bytes and, for a W2 stage, the h issuer's with the h bytes). The consumers compute
+//   from shared memory and release a stage on its "empty" mbarrier. The finisher turns the
+//   consumers' partial sums of a W13 stage into h (clamped SwiGLU) and stores it, the
+//   publisher makes it visible GPU-wide and counts it, and the h issuer copies h into the W2
+//   stages.
 //
 // * Work split. The active slots are the k routing slots (and the shared expert, slot 0); a
 //   slot whose id is invalid keeps its place with router weight 0, so the whole schedule is
@@ -24,8 +26,8 @@
 //   last one's. A W13 stage is one slot's share (or a part of it). For W2 each CTA owns a fixed
 //   block of output rows and streams those rows of every slot in the same order. A W2 stage of
 //   slot a needs all of h_a: once all 16 consumers have released a W13 stage, the finisher
-//   computes and stores the stage's h values and adds the stage's pairs to the slot's
-//   completion counter (one GPU-scope release per batch of stages); the h issuer waits
+//   computes and stores the stage's h values and the publisher adds the stage's pairs to the
+//   slot's completion counter (one GPU-scope release per batch of stages); the h issuer waits
 //   (acquire, bounded) until the counter of the slot a W2 run needs reaches I, then copies h_a
 //   into that stage with the bulk engine. There is no grid-wide barrier: W2 weights stream
 //   while W13 finishes, and each slot's W2 starts as soon as its own h is complete.
