@@ -66,7 +66,11 @@ DECODE_B8_E512 = LayerSpec("decode_t8_e512_k10_h4096_i1024_shared", seed=5, T=8,
                            H=4096, I=1024, logit_sigma=1.5, shared=True, instances=4)
 DECODE_B1_DEEP = LayerSpec("decode_t1_e8_k2_h8192_i4096", seed=6, T=1, E=8, k=2, H=8192,
                            I=4096, logit_sigma=1.0, instances=8)
-EXTRA_WORKLOADS = [DECODE_B8_E512, DECODE_B1_DEEP]
+DECODE_B16_E512 = LayerSpec("decode_t16_e512_k10_h4096_i1024_shared", seed=7, T=16, E=512, k=10,
+                            H=4096, I=1024, logit_sigma=1.5, shared=True, instances=4)
+DECODE_B8_DEEP = LayerSpec("decode_t8_e8_k2_h8192_i4096", seed=8, T=8, E=8, k=2, H=8192,
+                           I=4096, logit_sigma=1.0, instances=8)
+EXTRA_WORKLOADS = [DECODE_B8_E512, DECODE_B1_DEEP, DECODE_B16_E512, DECODE_B8_DEEP]
 BY_NAME = {s.name: s for s in WORKLOADS + EXTRA_WORKLOADS}
 
 

@@ -7,8 +7,8 @@ import pytest
 import torch
 
 from oracle import moe as om
-from synth import (DECODE_B1_DEEP, DECODE_B1_E288, DECODE_B1_E512, DECODE_B8_E512,
-                   DECODE_B32_E512, LayerSpec, make_layer)
+from synth import (DECODE_B1_DEEP, DECODE_B1_E288, DECODE_B1_E512, DECODE_B8_DEEP,
+                   DECODE_B8_E512, DECODE_B16_E512, DECODE_B32_E512, LayerSpec, make_layer)
 from synth.device import HostExperts, make_device_layer, nvfp4_experts
 from synth import philox as px
 from tests.layer_util import assert_close, bf16_to_f64, ftmoe, oracle_pool
@@ -84,3 +84,14 @@ def test_full_decode_t8_e512_shared_sampled():
 def test_full_decode_t1_few_large_experts():
     """Few, large experts: H = 8192, I = 4096 (eight k-steps per W13 row, four per W2 row)."""
     _device_parity(DECODE_B1_DEEP)
+
+
+def test_full_decode_t8_few_large_experts_every_row():
+    """A mid-size batch on few, large experts: every expert carries about two tokens and every
+    weight row a reduction of 8192 (W13) or 4096 (W2) elements; all 8 rows."""
+    _device_parity(DECODE_B8_DEEP, pool=True)
+
+
+def test_full_decode_t16_e512_shared_sampled():
+    """The 16-token batch of the 512-expert layer."""
+    _device_parity(DECODE_B16_E512, tokens=np.array([0, 5, 10, 15]))
