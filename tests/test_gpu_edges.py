@@ -46,6 +46,8 @@ def test_empty_batch():
 EDGE_CASES = [
     # the largest decode batch with the largest k (2048 token-expert pairs)
     (LayerSpec("t64_k32", seed=61, T=64, E=48, k=32, H=256, I=128), False),
+    # one token with the most slots: 32 routed + the shared expert
+    (LayerSpec("t1_k32_shared", seed=67, T=1, E=40, k=32, H=512, I=256, shared=True), False),
     # the largest H and the largest I the entry points accept
     (LayerSpec("h16384", seed=62, T=2, E=4, k=2, H=16384, I=128), False),
     (LayerSpec("i8192", seed=63, T=1, E=3, k=2, H=128, I=8192, shared=True), False),

@@ -17,6 +17,10 @@ CASES = [
     LayerSpec("r_t1_shared", seed=83, T=1, E=40, k=6, H=384, I=256, shared=True),
     LayerSpec("r_t1_k1", seed=84, T=1, E=5, k=1, H=256, I=128),
     LayerSpec("r_t5", seed=85, T=5, E=33, k=5, H=256, I=256, shared=True),       # two launches
+    # the most slots: 32 routed + the shared expert (33 active), ranked by counting
+    LayerSpec("r_t1_k32_sh", seed=86, T=1, E=48, k=32, H=256, I=128, shared=True),
+    # ... and with more than 512 experts (the route kernel's warp routine inside the kernel)
+    LayerSpec("r_t1_k32_e600", seed=87, T=1, E=600, k=32, H=256, I=128, shared=True),
 ]
 
 
