@@ -50,6 +50,7 @@ EDGE_CASES = [
     (LayerSpec("t1_k32_shared", seed=67, T=1, E=40, k=32, H=512, I=256, shared=True), False),
     # the largest H and the largest I the entry points accept
     (LayerSpec("h16384", seed=62, T=2, E=4, k=2, H=16384, I=128), False),
+    (LayerSpec("t1_h16384", seed=68, T=1, E=4, k=2, H=16384, I=128, shared=True), False),
     (LayerSpec("i8192", seed=63, T=1, E=3, k=2, H=128, I=8192, shared=True), False),
     # prefill at the same edges
     (LayerSpec("pf_k32", seed=64, T=100, E=64, k=32, H=256, I=128), True),
