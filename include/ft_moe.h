@@ -102,14 +102,17 @@ ft_status ft_moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
 
 /*
  * ft_moe_router_logits — the router's logits l_t = W_router x_t, and the shared expert's gate
- * dot x_t . gv in the same pass (the FreeToken commit log lists "moe router / shared gate"
- * kernels beside the MoE GEMV; the pages do not define them further: the plain reading is a
- * bf16 matrix-vector product with float32 accumulation).
+ * dot x_t . gv (the FreeToken commit log lists "moe router / shared gate" kernels beside the
+ * MoE GEMV; the pages do not define them further: the plain reading is a bf16 matrix product
+ * with float32 accumulation). Below 64 tokens one CUDA-core pass computes both; from 64 tokens
+ * the logits run on the tensor cores (one launch) and the gate dot on the CUDA cores (a second
+ * launch on the same stream).
  *   x         bf16 [T, H], w_router bf16 [E, H], gate bf16 [H] or NULL (16-byte aligned)
  *   logits    float [T, E] (4-byte aligned), fully overwritten
  *   gate_dot  float [T], written when gate is given (may be NULL otherwise)
  *   H a multiple of 8; E <= 4096. Products are exact in float32 and every sum runs in a fixed
- *   order (deterministic). T = 0 is a no-op.
+ *   order for a given T (deterministic; the two forms may differ in the last bits). T = 0 is a
+ *   no-op.
  */
 ft_status ft_moe_router_logits(const uint16_t* x, int32_t T, int32_t H, const uint16_t* w_router,
                                int32_t E, const uint16_t* gate, float* logits, float* gate_dot,

@@ -17,7 +17,10 @@ def _bits(a):
 
 
 CASES = [(1, 8, 256, False), (1, 288, 3072, False), (5, 512, 4096, True), (40, 64, 1024, True),
-         (300, 33, 520, True), (2048, 512, 4096, False)]
+         (300, 33, 520, True), (2048, 512, 4096, False),
+         # the tensor-core form (64 tokens and more): the first such T, a T one past a 128-token
+         # tile with partial expert tiles and a K tail, and the 2048-token batch with the gate
+         (64, 100, 1024, True), (129, 600, 776, False), (2048, 512, 4096, True)]
 
 
 @pytest.mark.parametrize("T,E,H,gate", CASES, ids=lambda c: str(c))
