@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--instances", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-streams", type=int, default=0,
-                    help="streams the end-to-end steps alternate over (default 2)")
+                    help="streams the end-to-end steps take in turn (default 3)")
     ap.add_argument("--only", action="store_true",
                     help="time the --workload alone (no companion configs)")
     ap.add_argument("--unrouted", action="store_true",
@@ -397,9 +397,10 @@ def run_e2e(args, spec, layers, exps, shs, ws, dev, bytes_call, world):
     hx = [torch.from_numpy(l.x_bits.view(np.int16).copy()).view(spec.T, spec.H).pin_memory()
           for l in layers[:n]]
     hl = [torch.from_numpy(np.ascontiguousarray(l.logits_np)).pin_memory() for l in layers[:n]]
-    # streams take alternate steps, each with its own device buffers and workspace, so one
-    # step's copies overlap the neighbouring step's kernels
-    nb = max(1, args.e2e_streams or 2)
+    # streams take the steps in turn, each with its own device buffers and workspace, so one
+    # step's copies overlap the neighbouring steps' kernels (with two, a step's input copy
+    # waits behind the output copy of the step two before it, on the same buffers)
+    nb = max(1, args.e2e_streams or 3)
     prefill = spec.prefill
     streams = [torch.cuda.Stream(device=dev) for _ in range(nb)]
     wss = [ws] + [ftmoe.new_workspace(spec.T, spec.k, exps[0], spec.shared, prefill=prefill)
