@@ -68,29 +68,23 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// One 64-element K chunk of two accumulators: D0 (+)= A0 * B and D1 (+)= A1 * B (kind::f16,
-// M=128, K=16 per product: four each; A_s at a_tmem + 32 s + 8 ks, B at b_desc + 32 bytes per
-// K step), issued by the whole converged warp with one elected lane issuing all eight. Issued
-// from a divergent single-thread branch instead, every product costs about twice as long.
-// acc = 0 starts both accumulators afresh.
-__device__ __forceinline__ void mma8_ts_warp(uint32_t d0, uint32_t d1, uint32_t a_tmem,
-                                             uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+// One 64-element K chunk of one accumulator: D (+)= A * B (kind::f16, M=128, K=16 per product:
+// four; A at a_tmem + 8 ks, B at b_desc + 32 bytes per K step), issued by the whole converged
+// warp with one elected lane issuing all four. Issued from a divergent single-thread branch
+// instead, every product costs about twice as long. acc = 0 starts the accumulator afresh.
+__device__ __forceinline__ void mma4_ts_warp(uint32_t d, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
-      "add.u32 a1, %2, 8;\n\tadd.u32 a2, %2, 16;\n\tadd.u32 a3, %2, 24;\n\t"
-      "add.u32 a4, %2, 32;\n\tadd.u32 a5, %2, 40;\n\tadd.u32 a6, %2, 48;\n\tadd.u32 a7, %2, 56;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %4, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, 1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, 1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, 1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a4], %3, %4, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a5], b1, %4, 1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a6], b2, %4, 1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a7], b3, %4, 1;\n\t}" ::"r"(d0),
-      "r"(d1), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, 1;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
       : "memory");
 }
 

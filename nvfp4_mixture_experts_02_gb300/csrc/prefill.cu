@@ -11,24 +11,26 @@
 //   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
 //                           part[pair], in slot order (deterministic), bf16 out
 //
-// k_pf_gemm is persistent (one CTA per SM, 16 producer warps and one MMA warp). A work item is
+// k_pf_gemm is persistent (one CTA per SM, 16 producer warps and two MMA warps). A work item is
 // one token group of one expert (up to 128 tokens, the MMA N) against 256 weight rows: for W13
 // the 128 gate rows and the 128 matching up rows of a row block (two fp32 accumulators in
 // tensor memory, so SwiGLU pairs land in the same TMEM lane), for W2 two 128-row blocks of the
 // output. The item's weight codes arrive as tiles of 4 chunks (256 rows x 128 bytes) through
 // the tensor-memory-access engine (two 2D tensor-map copies per tile, 128-byte swizzle, three
-// tile slots), sent by the MMA warp once every producer is past the tile the slot held. Two
+// tile slots), sent by the first MMA warp once every producer is past the tile the slot held. Two
 // producer threads share each weight row, each owning half of every chunk (32 elements): it
 // reads its 16 code bytes from the tile, takes its two E4M3 scales through a small register
 // pipeline (L1-allocating loads), forms e2m1*e4m3 exactly in f16 (hardware conversions + one
 // f16x2 multiply per pair) and writes it into tensor memory (tcgen05.st) as the MMA's A
 // operand. The group's activations (B operand) go straight from global to shared memory by
 // cp.async, in the canonical K-major core-matrix layout, 4 chunks ahead in 8 stages. Every
-// producer arrives on the stage's "full" mbarrier when its part of a chunk is in place; the MMA
-// warp waits for the stage and, as a whole converged warp with one elected lane, issues
-// tcgen05.mma (kind::f16, A from TMEM, B from shared memory, M=128, N = group size rounded up
-// to 16, K=16 per instruction), committing to the stage's "done" mbarrier. Four stages and no
-// CTA-wide barrier per chunk let the producers run ahead of the MMAs.
+// producer arrives on the stage's "full" mbarrier when its part of a chunk is in place; each MMA
+// warp waits for the stage and, as a whole converged warp with one elected lane, issues the
+// tcgen05.mma products of its accumulator (kind::f16, A from TMEM, B from shared memory, M=128,
+// N = group size rounded up to 16, K=16 per instruction; the first warp into the gate / first
+// output-row accumulator, the second into the other, so the two issue side by side),
+// committing to the stage's "done" mbarrier. Four stages and no CTA-wide barrier per chunk let
+// the producers run ahead of the MMAs.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -44,7 +46,7 @@ namespace ftmoe {
 namespace {
 
 constexpr int kPfProducers = 512;        // 16 producer warps: two threads per weight row
-constexpr int kPfThreads = kPfProducers + 32;   // + one warp that issues the MMAs
+constexpr int kPfThreads = kPfProducers + 64;   // + two warps that issue the MMAs
 constexpr int kPfN = 112;                // max tokens per group (MMA N; shared memory sets it)
 constexpr int kPfKc = 64;                // reduction elements per chunk (32 packed bytes)
 constexpr int kPfStages = 4;              // pipeline stages = chunks in flight per thread
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&mbar_full[s], kPfProducers);
-      mbar_init(&mbar_done[s], 1);
+      mbar_init(&mbar_done[s], 2);   // one commit per MMA warp
     }
     for (int s = 0; s < kPfWTiles; ++s) mbar_init(&mbar_w[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -474,11 +476,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
     };
     const uint32_t idesc = idesc_f16(128, npad);
     if (!producer) {
-      // ---- MMA warp: sends the item's code tiles (the first three now; tile t + 3 once
+      // ---- MMA warps: mw 0 sends the item's code tiles (the first three now; tile t + 3 once
       // every producer is past tile t, i.e. the "full" barrier of its last chunk has
-      // completed), and for each chunk waits until every producer has filled the stage,
-      // issues its MMAs and commits them to the stage's "done" barrier
-      if (lane == 0)
+      // completed) and issues the products into D0 (gate rows / first output rows), mw 1 those
+      // into D1; for each chunk each waits until every producer has filled the stage, issues
+      // its four products and commits them to the stage's "done" barrier (two commits a phase)
+      const int mw = warp - kPfProducers / 32;
+      if (mw == 0 && lane == 0)
         for (int t = 0; t < kPfWTiles && t < ntiles; ++t) issue_tile(t);
       __syncwarp();
       for (int c = 0; c < nchunks && ok; ++c) {
@@ -486,14 +490,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(const __grid_constant
         ok = mbar_wait(&mbar_full[st], (nprod / kPfStages) & 1, p.err, kErrTimeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         const int t = c / kPfTileChunks;
-        if (lane == 0 && ok && (c % kPfTileChunks == kPfTileChunks - 1 || c == nchunks - 1) &&
-            t + kPfWTiles < ntiles)
+        if (mw == 0 && lane == 0 && ok &&
+            (c % kPfTileChunks == kPfTileChunks - 1 || c == nchunks - 1) && t + kPfWTiles < ntiles)
           issue_tile(t + kPfWTiles);
         __syncwarp();
         tc_fence_after();
         {   // the whole warp passes the operands, one elected lane issues
           const uint32_t b0 = smem_addr(sB + (int)(nprod % kPfBStages) * kBTileBytes);
-          mma8_ts_warp(tbase + kColD0, tbase + kColD1, tbase + kColA + (uint32_t)st * 64,
+          mma4_ts_warp(tbase + (mw == 0 ? kColD0 : kColD1),
+                       tbase + kColA + (uint32_t)st * 64 + 32u * (uint32_t)mw,
                        smem_desc_sw128(b0, 1024), idesc, c > 0 ? 1u : 0u);
           mma_commit_warp(&mbar_done[st]);
         }
