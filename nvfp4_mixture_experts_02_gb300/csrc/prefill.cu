@@ -85,27 +85,47 @@ struct PfPlanArgs {
   int max_groups;
 };
 
+// Slot j of token t keeps expert e when e is in [0, E) and no earlier slot of the token holds
+// it. The earlier slots are read without early exit, so their loads overlap.
+__device__ __forceinline__ bool plan_slot_ok(const int* idx, int t, int j, int k, int e, int E) {
+  bool rep = false;
+#pragma unroll 4
+  for (int jj = 0; jj < j; ++jj) rep |= __ldg(idx + (size_t)t * k + jj) == e;
+  return e >= 0 && e < E && !rep;
+}
+
 // The grouping runs in one CTA; pair positions inside an expert come from shared-memory
 // atomics (their order is not reproducible, but every pair's value is computed from its
-// own token only and the final sum runs in slot order, so the output bits are).
+// own token only and the final sum runs in slot order, so the output bits are). Per expert,
+// the first pair and the W2 scale ratio are kept in shared memory, so placing a pair reads
+// nothing back from global memory.
 __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
-  __shared__ int cnt[kMaxExperts + 1];       // pair counts, then fill counters
-  __shared__ int act_of_e[kMaxExperts + 1];
+  extern __shared__ int plan_sm[];
+  int* cnt = plan_sm;                                  // [E] pair counts, then fill counters
+  int* pair0_of_e = plan_sm + p.E;                     // [E] first pair of an active expert
+  float* ratio_of_e = reinterpret_cast<float*>(plan_sm + 2 * p.E);   // [E] g2 / g2ref
   __shared__ float red[32];
   griddep_launch_dependents();
   griddep_wait();
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int T = p.T, k = p.k, E = p.E, TK = T * k;
   const bool has_shared = p.sh_g2 != nullptr;
-  for (int e = tid; e <= E; e += nthr) cnt[e] = 0;
+  for (int e = tid; e < E; e += nthr) cnt[e] = 0;
   __syncthreads();
-  for (int q = tid; q < TK; q += nthr) {
-    const int t = q / k, j = q - t * k;
-    const int e = p.topk_idx[q];
-    bool ok = e >= 0 && e < E;
-    for (int jj = 0; jj < j && ok; ++jj) ok = p.topk_idx[t * k + jj] != e;
-    if (ok) atomicAdd(&cnt[e], 1);
-    else atomicOr(p.err, kErrBadExpert);
+  // four pairs per thread at a time: their ids are loaded together
+  for (int q0 = tid; q0 < TK; q0 += 4 * nthr) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ev[u] = q0 + u * nthr < TK ? __ldg(p.topk_idx + q0 + u * nthr) : 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + u * nthr;
+      if (q < TK) {
+        const int t = q / k, j = q - t * k;
+        if (plan_slot_ok(p.topk_idx, t, j, k, ev[u], E)) atomicAdd(&cnt[ev[u]], 1);
+        else atomicOr(p.err, kErrBadExpert);
+      }
+    }
   }
   __syncthreads();
   // active experts in ascending id order (serial scan by warp 0: E <= 4096)
@@ -130,7 +150,7 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
       }
       if (f) {
         const int a = base_a + ia - 1, p0 = base_p + ip - c, g0 = base_g + ig - ng;
-        act_of_e[e] = a;
+        pair0_of_e[e] = p0;
         p.act_expert[a] = e;
         p.act_pair0[a] = p0;
         for (int g = 0; g < ng; ++g) {
@@ -138,8 +158,6 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
           p.group_p0[g0 + g] = p0 + g * kPfN;
           p.group_n[g0 + g] = min(kPfN, c - g * kPfN);
         }
-      } else if (e < E) {
-        act_of_e[e] = -1;
       }
       base_a += __shfl_sync(0xffffffffu, ia, 31);
       base_p += __shfl_sync(0xffffffffu, ip, 31);
@@ -168,10 +186,10 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
     }
   }
   __syncthreads();
-  const int n_routed = p.hdr[4];
-  // reference W2 tensor scale
+  // reference W2 tensor scale: the largest over the active experts
   float gmax = 0.f;
-  for (int i = tid; i < n_routed; i += nthr) gmax = fmaxf(gmax, p.g2[p.act_expert[i]]);
+  for (int e = tid; e < E; e += nthr)
+    if (cnt[e] > 0) gmax = fmaxf(gmax, p.g2[e]);
   if (tid == 0 && has_shared) gmax = fmaxf(gmax, *p.sh_g2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
@@ -188,27 +206,40 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
   }
   __syncthreads();
   const float g2ref = red[0];
-  int* fill = cnt;   // counts are no longer needed: reuse them as fill counters
-  for (int e = tid; e <= E; e += nthr) fill[e] = 0;
+  for (int e = tid; e < E; e += nthr)
+    if (cnt[e] > 0) ratio_of_e[e] = p.g2[e] / g2ref;
   __syncthreads();
-  // place the pairs
-  for (int q = tid; q < TK; q += nthr) {
-    const int t = q / k, j = q - t * k;
-    const int e = p.topk_idx[q];
-    bool ok = e >= 0 && e < E;
-    for (int jj = 0; jj < j && ok; ++jj) ok = p.topk_idx[t * k + jj] != e;
-    if (!ok) {
-      p.pair_slot[q] = -1;
-      continue;
+  int* fill = cnt;   // counts are no longer needed: reuse them as fill counters
+  for (int e = tid; e < E; e += nthr) fill[e] = 0;
+  __syncthreads();
+  // place the pairs, four per thread at a time
+  for (int q0 = tid; q0 < TK; q0 += 4 * nthr) {
+    int ev[4];
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool in = q0 + u * nthr < TK;
+      ev[u] = in ? __ldg(p.topk_idx + q0 + u * nthr) : 0;
+      wv[u] = in ? __ldg(p.topk_w + q0 + u * nthr) : 0.f;
     }
-    const int a = act_of_e[e];
-    const int pos = p.act_pair0[a] + atomicAdd(&fill[e], 1);
-    p.pair_tok[pos] = t;
-    p.pair_w[pos] = p.topk_w[q] * (p.g2[e] / g2ref) * p.hscale;
-    p.pair_slot[q] = pos;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + u * nthr;
+      if (q < TK) {
+        const int t = q / k, j = q - t * k, e = ev[u];
+        if (!plan_slot_ok(p.topk_idx, t, j, k, e, E)) {
+          p.pair_slot[q] = -1;
+        } else {
+          const int pos = pair0_of_e[e] + atomicAdd(&fill[e], 1);
+          p.pair_tok[pos] = t;
+          p.pair_w[pos] = wv[u] * ratio_of_e[e] * p.hscale;
+          p.pair_slot[q] = pos;
+        }
+      }
+    }
   }
   if (has_shared) {
-    const int pr0 = p.act_pair0[n_routed];
+    const int pr0 = p.hdr[2] - T;   // the shared expert's pairs come last
     for (int t = tid; t < T; t += nthr) p.pair_tok[pr0 + t] = t;
   }
 }
@@ -763,7 +794,18 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   pa.max_groups = L.max_groups;
   {
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = pdl_cfg(dim3(1), dim3(1024), 0, stream, at);
+    const size_t plan_smem = (size_t)3 * ex.E * sizeof(int);
+    static std::atomic<bool> plan_attr[64];   // per device: up to 3 * kMaxExperts ints
+    int pdev = 0;
+    if ((err = cudaGetDevice(&pdev)) != cudaSuccess) return err;
+    if (pdev < 0 || pdev >= 64) return cudaErrorInvalidDevice;
+    if (!plan_attr[pdev].load(std::memory_order_relaxed)) {
+      if ((err = cudaFuncSetAttribute(k_pf_plan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      3 * kMaxExperts * (int)sizeof(int))) != cudaSuccess)
+        return err;
+      plan_attr[pdev].store(true, std::memory_order_relaxed);
+    }
+    cudaLaunchConfig_t cfg = pdl_cfg(dim3(1), dim3(1024), plan_smem, stream, at);
     if ((err = cudaLaunchKernelEx(&cfg, k_pf_plan, pa)) != cudaSuccess) return err;
   }
   PfActArgs aa;
