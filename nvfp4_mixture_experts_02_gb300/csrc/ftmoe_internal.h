@@ -66,7 +66,7 @@ struct PrefillLayout {
   int max_pairs = 0, max_groups = 0;
   size_t err = 0, hdr = 0, act_expert = 0, act_pair0 = 0, group_act = 0, group_p0 = 0,
          group_n = 0, pair_tok = 0, pair_w = 0, pair_slot = 0, xf = 0, xscale = 0, h = 0,
-         part = 0, total = 0;
+         part = 0, e_pair0 = 0, e_ratio = 0, e_fill = 0, total = 0;
   PrefillLayout(int T, int k, int E, int H, int I, bool shared);
 };
 

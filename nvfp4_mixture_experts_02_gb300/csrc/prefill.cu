@@ -2,10 +2,11 @@
 // contractions on the 5th-generation tensor cores (tcgen05), which is where a
 // multi-token chunk has enough reuse per weight to need them.
 //
-//   k_pf_plan    (1 CTA)    group the (token, slot) pairs by expert; token groups of at
-//                           most 128 per expert; pair weights; per-token slot -> pair map
-//   k_pf_act     (T warps)  f16 activations with a per-token power-of-two scale, and the
-//                           shared-expert gate
+//   k_pf_plan    (1 CTA)    count the (token, slot) pairs per expert; the experts' first
+//                           pairs, token groups of at most 112 per expert, W2 scale ratios
+//   k_pf_act     (T warps)  place each token's pairs (pair weights, per-token slot -> pair
+//                           map); f16 activations with a per-token power-of-two scale, and
+//                           the shared-expert gate
 //   k_pf_gemm<W13>          h[pair, I] = SwiGLU(G x, U x) * pair weight (f16)
 //   k_pf_gemm<W2>           part[pair, H] = W2 h (fp32), per pair
 //   k_pf_reduce             y[t] = sum over the token's slots (and the shared expert) of
@@ -82,6 +83,9 @@ struct PfPlanArgs {
   int* pair_tok;        // [P]
   float* pair_w;        // [P]
   int* pair_slot;       // [T*k]: pair of (token, slot), -1 if the slot was invalid
+  int* e_pair0;         // [E] first pair of each active expert (for the activation kernel)
+  float* e_ratio;       // [E] its W2 tensor scale / the reference
+  int* e_fill;          // [E] pairs placed so far (zeroed here)
   int max_groups;
 };
 
@@ -96,14 +100,12 @@ __device__ __forceinline__ bool plan_slot_ok(const int* idx, int t, int j, int k
 
 // The grouping runs in one CTA; pair positions inside an expert come from shared-memory
 // atomics (their order is not reproducible, but every pair's value is computed from its
-// own token only and the final sum runs in slot order, so the output bits are). Per expert,
-// the first pair and the W2 scale ratio are kept in shared memory, so placing a pair reads
-// nothing back from global memory.
+// own token only and the final sum runs in slot order, so the output bits are). The pairs
+// themselves are placed by the activation kernel, one warp per token, across the GPU.
 __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
   extern __shared__ int plan_sm[];
-  int* cnt = plan_sm;                                  // [E] pair counts, then fill counters
+  int* cnt = plan_sm;                                  // [E] pair counts
   int* pair0_of_e = plan_sm + p.E;                     // [E] first pair of an active expert
-  float* ratio_of_e = reinterpret_cast<float*>(plan_sm + 2 * p.E);   // [E] g2 / g2ref
   __shared__ float red[32];
   griddep_launch_dependents();
   griddep_wait();
@@ -206,37 +208,14 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
   }
   __syncthreads();
   const float g2ref = red[0];
-  for (int e = tid; e < E; e += nthr)
-    if (cnt[e] > 0) ratio_of_e[e] = p.g2[e] / g2ref;
-  __syncthreads();
-  int* fill = cnt;   // counts are no longer needed: reuse them as fill counters
-  for (int e = tid; e < E; e += nthr) fill[e] = 0;
-  __syncthreads();
-  // place the pairs, four per thread at a time
-  for (int q0 = tid; q0 < TK; q0 += 4 * nthr) {
-    int ev[4];
-    float wv[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool in = q0 + u * nthr < TK;
-      ev[u] = in ? __ldg(p.topk_idx + q0 + u * nthr) : 0;
-      wv[u] = in ? __ldg(p.topk_w + q0 + u * nthr) : 0.f;
+  // per active expert: first pair and W2 scale ratio, for the activation kernel that places
+  // the pairs; its fill counters start at zero
+  for (int e = tid; e < E; e += nthr) {
+    if (cnt[e] > 0) {
+      p.e_pair0[e] = pair0_of_e[e];
+      p.e_ratio[e] = p.g2[e] / g2ref;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int q = q0 + u * nthr;
-      if (q < TK) {
-        const int t = q / k, j = q - t * k, e = ev[u];
-        if (!plan_slot_ok(p.topk_idx, t, j, k, e, E)) {
-          p.pair_slot[q] = -1;
-        } else {
-          const int pos = pair0_of_e[e] + atomicAdd(&fill[e], 1);
-          p.pair_tok[pos] = t;
-          p.pair_w[pos] = wv[u] * ratio_of_e[e] * p.hscale;
-          p.pair_slot[q] = pos;
-        }
-      }
-    }
+    p.e_fill[e] = 0;
   }
   if (has_shared) {
     const int pr0 = p.hdr[2] - T;   // the shared expert's pairs come last
@@ -246,7 +225,14 @@ __global__ void __launch_bounds__(1024) k_pf_plan(const PfPlanArgs p) {
 
 struct PfActArgs {
   const uint16_t* x;
-  int T, H;
+  int T, H, k, E;
+  const int* topk_idx;    // [T, k]
+  const float* topk_w;
+  const int* e_pair0;     // the plan's per-expert first pairs and W2 ratios
+  const float* e_ratio;
+  int* e_fill;
+  int* pair_tok;
+  int* pair_slot;
   const uint16_t* sh_gate;
   const float* sh_g2;
   float hscale;
@@ -257,14 +243,35 @@ struct PfActArgs {
   float* xscale;
 };
 
-// One warp per token: f16 copy of x scaled so that max |x| is in [2^14, 2^15), and the
-// shared expert's weight sigmoid(x . gv) * (W2 scale ratio) * 2^S.
+// One warp per token: its pairs placed (lane j takes slot j: a position in its expert's pair
+// range, the pair's token and weight w * (W2 scale ratio) * 2^S, the slot -> pair map), f16
+// copy of x scaled so that max |x| is in [2^14, 2^15), and the shared expert's weight
+// sigmoid(x . gv) * (W2 scale ratio) * 2^S.
 __global__ void __launch_bounds__(256) k_pf_act(const PfActArgs p) {
   griddep_launch_dependents();
   griddep_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= p.T) return;
+  {
+    const size_t q = (size_t)t * p.k + lane;
+    const int e = lane < p.k ? p.topk_idx[q] : -1;
+    bool rep = false;   // an earlier slot of the token holds the same expert
+    for (int jj = 0; jj < p.k; ++jj) {
+      const int ej = __shfl_sync(0xffffffffu, e, jj);
+      rep |= jj < lane && ej == e;
+    }
+    if (lane < p.k) {
+      if (e >= 0 && e < p.E && !rep) {
+        const int pos = p.e_pair0[e] + atomicAdd(p.e_fill + e, 1);
+        p.pair_tok[pos] = t;
+        p.pair_w[pos] = p.topk_w[q] * p.e_ratio[e] * p.hscale;
+        p.pair_slot[q] = pos;
+      } else {
+        p.pair_slot[q] = -1;
+      }
+    }
+  }
   const uint16_t* xr = p.x + (size_t)t * p.H;
   float amax = 0.f, dot = 0.f;
   for (int c = lane * 8; c < p.H; c += 256) {
@@ -718,6 +725,9 @@ PrefillLayout::PrefillLayout(int T, int k, int E, int H, int I, bool shared) {
   xscale = take(4 * (size_t)T);
   h = take(2 * (size_t)max_pairs * I);
   part = take(4 * (size_t)max_pairs * H);
+  e_pair0 = take(4 * (size_t)E);
+  e_ratio = take(4 * (size_t)E);
+  e_fill = take(4 * (size_t)E);
   total = o;
 }
 
@@ -791,17 +801,18 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
   pa.hdr = I32(L.hdr); pa.act_expert = I32(L.act_expert); pa.act_pair0 = I32(L.act_pair0);
   pa.group_act = I32(L.group_act); pa.group_p0 = I32(L.group_p0); pa.group_n = I32(L.group_n);
   pa.pair_tok = I32(L.pair_tok); pa.pair_w = F32(L.pair_w); pa.pair_slot = I32(L.pair_slot);
+  pa.e_pair0 = I32(L.e_pair0); pa.e_ratio = F32(L.e_ratio); pa.e_fill = I32(L.e_fill);
   pa.max_groups = L.max_groups;
   {
     cudaLaunchAttribute at[1];
-    const size_t plan_smem = (size_t)3 * ex.E * sizeof(int);
-    static std::atomic<bool> plan_attr[64];   // per device: up to 3 * kMaxExperts ints
+    const size_t plan_smem = (size_t)2 * ex.E * sizeof(int);
+    static std::atomic<bool> plan_attr[64];   // per device: up to 2 * kMaxExperts ints
     int pdev = 0;
     if ((err = cudaGetDevice(&pdev)) != cudaSuccess) return err;
     if (pdev < 0 || pdev >= 64) return cudaErrorInvalidDevice;
     if (!plan_attr[pdev].load(std::memory_order_relaxed)) {
       if ((err = cudaFuncSetAttribute(k_pf_plan, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      3 * kMaxExperts * (int)sizeof(int))) != cudaSuccess)
+                                      2 * kMaxExperts * (int)sizeof(int))) != cudaSuccess)
         return err;
       plan_attr[pdev].store(true, std::memory_order_relaxed);
     }
@@ -809,7 +820,10 @@ cudaError_t launch_prefill(const uint16_t* x, int T, const int* topk_idx, const 
     if ((err = cudaLaunchKernelEx(&cfg, k_pf_plan, pa)) != cudaSuccess) return err;
   }
   PfActArgs aa;
-  aa.x = x; aa.T = T; aa.H = ex.H; aa.sh_gate = shared ? ex.sh_gate : nullptr;
+  aa.x = x; aa.T = T; aa.H = ex.H; aa.k = k; aa.E = ex.E; aa.topk_idx = topk_idx;
+  aa.topk_w = topk_w; aa.e_pair0 = I32(L.e_pair0); aa.e_ratio = F32(L.e_ratio);
+  aa.e_fill = I32(L.e_fill); aa.pair_tok = I32(L.pair_tok); aa.pair_slot = I32(L.pair_slot);
+  aa.sh_gate = shared ? ex.sh_gate : nullptr;
   aa.sh_g2 = shared ? ex.sh_g2 : nullptr; aa.hscale = hscale; aa.hdr = I32(L.hdr);
   aa.act_pair0 = I32(L.act_pair0); aa.pair_w = F32(L.pair_w);
   aa.xf = reinterpret_cast<__half*>(base + L.xf); aa.xscale = F32(L.xscale);
